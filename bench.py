@@ -1,0 +1,396 @@
+"""Benchmark of the fused AdamW step with compressed moment state.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                [--workload flat_16m] [--modes q8,bf16m,fp32] [--no-cpu-baseline]
+
+One step = one call of the library over the workload's whole tensor list (load, dequantize,
+AdamW, requantize, store: a single kernel launch per <=440 tensors). The headline workload
+is the 8-bit block-wise AdamW step on one fp32 tensor of 16,777,216 params (block 2048,
+round to nearest, grads ~N(0, 1e-3^2)); the JSON line also reports the same tensor with
+bf16 and fp32 moments. Inputs are synthetic and seeded (workloads.py) and resident in
+HBM before the timed region; 8 distinct grad sets are cycled. Between timed steps the L2
+is flushed by writing a 384 MB buffer, outside the per-step CUDA events.
+
+value      = params updated per second over all ranks (Gparams/s), device-timed
+e2e        = the same through the public API with host buffers: each step copies its grads
+             from pinned host memory and the updated params back, inside the timed span
+roofline   = algorithmic HBM bytes per launch / mean launch time vs MEASURED_PEAKS.json
+cpu_baseline = the CPU oracle (single thread) on a bounded sample of the workload
+
+Under torchrun (N > 1) every rank runs its own shard of the same size on its own GPU
+(weak scaling, no collective in the step); the time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "Gparams/s per AdamW step and achieved HBM GB/s (% of GB300 peak), per moment mode"
+L2_FLUSH_BYTES = 384 << 20
+STATE_BYTES = {"fp32": 4, "bf16m": 2, "q8": 1}   # per moment element
+
+
+def algorithmic_bytes(mode: str, sizes, grad_dtype: str) -> int:
+    """Bytes the step must move once each: p read+write, g read, m and v read+write,
+    and for 8-bit moments the two fp32 scales of every block read+write."""
+    g = 4 if grad_dtype == "f32" else 2
+    per = 8 + g + 4 * STATE_BYTES[mode]
+    total = per * sum(sizes)
+    if mode == "q8":
+        total += 16 * sum((n + 2047) // 2048 for n in sizes)
+    return total
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "precision_state_adam_gb300", "csrc", "*"))):
+        with open(f, "rb") as fh:
+            h.update(os.path.basename(f).encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def ncu_traffic(workload: str, mode: str):
+    """Per-launch DRAM bytes from the committed ncu summary, if the kernel sources have
+    not changed since it was captured."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    e = d.get(f"{workload}/{mode}")
+    if not e or e.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------------ clocks during the timed region
+class ClockSampler:
+    FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str | None):
+        self.uuid = uuid
+        self.rows = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 8:
+                self.rows.append(parts)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=5)
+        rows = [r for r in self.rows if self.uuid is None or self.uuid in r[0]] or self.rows
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({n for r in rows for n, v in zip(names, r[4:8]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ our implementation
+def run_ours(args, rank: int, world: int, dist):
+    import torch
+    import precision_state_adam_gb300 as psa
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    w = workloads.WORKLOADS[args.workload]
+    sizes = w.sizes
+    numel = sum(sizes)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    n_sets = min(8, args.steps + args.warmup)
+    gdt = torch.float32 if w.grad_dtype == "f32" else torch.bfloat16
+    grads = []
+    for s in range(n_sets):
+        grads.append(workloads.grads_torch(sizes, s + 1, w.grad_std, dev, seed=workloads.DEFAULT_SEED + 1000 * rank,
+                                           kind=w.grad_kind, dtype=w.grad_dtype))
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        uuid = None
+    clocks = ClockSampler(uuid)
+    clocks.start()
+    results = {}
+    modes = args.modes
+    for mode in modes:
+        params = workloads.init_params_torch(w.specs, dev, seed=workloads.DEFAULT_SEED + rank)
+        state = psa.zeros_state(params, mode)
+        kw = dict(lr=w.lr, beta1=w.beta1, beta2=w.beta2, eps=w.eps, weight_decay=w.weight_decay)
+        if mode == "q8":
+            kw.update(stochastic_rounding=w.stochastic_rounding, seed=w.seed, percentile=w.percentile)
+        launches_per_step = -(-len([n for n in sizes if n > 0]) // (8 if len(sizes) <= 8 else 440))
+        t = 0
+        for _ in range(args.warmup):
+            t += 1
+            psa.adam_step(mode, params, grads[(t - 1) % n_sets], state, t, **kw)
+        torch.cuda.synchronize(dev)
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        evs = []
+        for _ in range(args.steps):
+            t += 1
+            flush.fill_(float(t))
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            psa.adam_step(mode, params, grads[(t - 1) % n_sets], state, t, **kw)
+            e1.record(stream)
+            evs.append((e0, e1))
+        torch.cuda.synchronize(dev)
+        if dist is not None:
+            dist.barrier()
+        step_ms = [a.elapsed_time(b) for a, b in evs]
+        total_s = sum(step_ms) / 1e3
+        if dist is not None:
+            tt = torch.tensor([total_s], dtype=torch.float64, device=dev)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            total_s = float(tt.item())
+        nbytes = algorithmic_bytes(mode, sizes, w.grad_dtype)
+        mean_s = sum(step_ms) / len(step_ms) / 1e3
+        results[mode] = {
+            "gparams_per_s": world * numel * args.steps / total_s / 1e9,
+            "ms_per_step": total_s * 1e3 / args.steps,
+            "median_ms": statistics.median(step_ms),
+            "bytes_per_step": nbytes,
+            "achieved_gbs": nbytes / mean_s / 1e9,
+            "launches": launches_per_step * args.steps,
+        }
+        # ---- end to end through the public API with host buffers
+        if mode == args.modes[0]:
+            results[mode]["e2e"] = run_e2e(args, psa, torch, dev, stream, w, params, state, kw, t, flush, dist, world)
+            results[mode]["launches"] += launches_per_step * args.steps
+        del params, state
+        torch.cuda.empty_cache()
+    clk = clocks.stop()
+    return results, clk
+
+
+def run_e2e(args, psa, torch, dev, stream, w, params, state, kw, t, flush, dist, world):
+    sizes = w.sizes
+    gdt = torch.float32 if w.grad_dtype == "f32" else torch.bfloat16
+    host_g = [workloads.grads_torch(sizes, s + 1, w.grad_std, dev, dtype=w.grad_dtype) for s in range(2)]
+    host_g = [[g.cpu().pin_memory() for g in gs] for gs in host_g]
+    host_p = [torch.empty(p.numel(), dtype=torch.float32, pin_memory=True) for p in params]
+    dev_g = [torch.empty(n, dtype=gdt, device=dev) for n in sizes]
+    h2d = sum(g.numel() * g.element_size() for g in host_g[0])
+    d2h = sum(p.numel() * 4 for p in params)
+    for i in range(3):  # warm the copy engines
+        t += 1
+        for d, h in zip(dev_g, host_g[i % 2]):
+            d.copy_(h, non_blocking=True)
+        psa.adam_step(args.modes[0], params, dev_g, state, t, **kw)
+        for h, p in zip(host_p, params):
+            h.copy_(p, non_blocking=True)
+    torch.cuda.synchronize(dev)
+    if dist is not None:
+        dist.barrier()
+    ms = []
+    for i in range(args.steps):
+        t += 1
+        flush.fill_(float(t))
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for d, h in zip(dev_g, host_g[i % 2]):
+            d.copy_(h, non_blocking=True)
+        psa.adam_step(args.modes[0], params, dev_g, state, t, **kw)
+        for h, p in zip(host_p, params):
+            h.copy_(p, non_blocking=True)
+        e1.record(stream)
+        e1.synchronize()
+        ms.append(e0.elapsed_time(e1))
+    total_s = sum(ms) / 1e3
+    if dist is not None:
+        tt = torch.tensor([total_s], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_s = float(tt.item())
+    return {"value": round(world * sum(sizes) * args.steps / total_s / 1e9, 3), "unit": "Gparams/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+# ------------------------------------------------------------------ the CPU oracle as a baseline
+def oracle_sample_rate(w: workloads.Workload, mode: str, budget_s: float):
+    """Time the CPU oracle (as it is: plain scalar C, one thread) on whole 2048-element
+    blocks of the workload's first tensor, step after step, for about `budget_s` seconds."""
+    import numpy as np
+    import oracle
+
+    n = min(w.sizes[0], 256 * 2048)
+    rng = np.random.default_rng(0)
+    p = (rng.standard_normal(n) * 0.02).astype(np.float32)
+    if mode == "fp32":
+        st = [np.zeros(n, np.float32), np.zeros(n, np.float32)]
+    elif mode == "bf16m":
+        st = [np.zeros(n, np.uint16), np.zeros(n, np.uint16)]
+    else:
+        nb = oracle.n_blocks(n)
+        st = [np.zeros(n, np.int8), np.zeros(n, np.uint8), np.zeros(nb, np.float32), np.zeros(nb, np.float32)]
+    g = (rng.standard_normal(n) * w.grad_std).astype(np.float32)
+    if w.grad_dtype == "bf16":
+        g = (g.view(np.uint32) >> 16).astype(np.uint16)
+    hp = oracle.HParams(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay)
+    q8 = oracle.Q8Opts(w.stochastic_rounding, w.seed, w.percentile)
+    done, t, t0 = 0, 0, time.perf_counter()
+    while True:
+        t += 1
+        oracle.step_list(mode, [p], [g], [st], t, hp, q8)
+        done += n
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    return done / el / 1e9, f"{t} steps over the first {n:,} params of the workload ({n // 2048} blocks), " \
+                            f"{el:.1f} s, one thread"
+
+
+def run_reference(args, rank, world):
+    """The reference arm: the CPU oracle, as it stands, on this machine's host cores."""
+    w = workloads.WORKLOADS[args.workload]
+    mode = args.modes[0]
+    times = []
+    vals = []
+    for _ in range(args.warmup):
+        oracle_sample_rate(w, mode, 0.5)
+    sample = ""
+    for _ in range(args.steps):
+        v, sample = oracle_sample_rate(w, mode, args.ref_step_seconds)
+        vals.append(v)
+    value = statistics.median(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "Gparams/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(sum(w.sizes) / (value * 1e9) * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.name, "description": w.description, "moment_mode": mode, "params": sum(w.sizes)},
+        "cpu_baseline": {"value": round(value, 6), "unit": "Gparams/s", "cores": 1, "kind": "oracle",
+                         "sample": f"each step: {sample}"},
+        "e2e": {"value": round(value, 6), "unit": "Gparams/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="flat_16m", choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--modes", default=None, help="comma list; the first is the headline (default: workload's)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-step-seconds", type=float, default=3.0)
+    args = ap.parse_args()
+    w = workloads.WORKLOADS[args.workload]
+    if args.modes is None:
+        rest = [m for m in ("q8", "bf16m", "fp32") if m != w.mode]
+        args.modes = [w.mode] + rest
+    else:
+        args.modes = args.modes.split(",")
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            run_reference(args, rank, world)
+        return
+
+    dist = None
+    if world > 1:
+        import torch
+        import torch.distributed as tdist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        tdist.init_process_group("nccl")
+        dist = tdist
+    results, clk = run_ours(args, rank, world, dist)
+    if rank == 0:
+        head = args.modes[0]
+        r = results[head]
+        peak, peak_kind = measured_peaks()
+        cpu = None
+        if world == 1 and not args.no_cpu_baseline:
+            v, sample = oracle_sample_rate(w, head, args.cpu_seconds)
+            cpu = {"value": round(v, 6), "unit": "Gparams/s", "cores": 1, "kind": "oracle", "sample": sample}
+        traffic = ncu_traffic(w.name, head)
+        line = {
+            "metric": METRIC, "value": round(r["gparams_per_s"], 3), "unit": "Gparams/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(r["ms_per_step"], 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": w.name, "description": w.description, "moment_mode": head,
+                       "params": sum(w.sizes), "tensors": len(w.sizes), "grad_dtype": w.grad_dtype,
+                       "bytes_per_step": r["bytes_per_step"],
+                       "l2": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MB write outside the step events)",
+                       "grads": "8 seeded sets resident in HBM, cycled"},
+            "roofline": {"bound": "hbm", "achieved": round(r["achieved_gbs"], 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(r["achieved_gbs"] / peak, 4), "peak_kind": peak_kind,
+                         "traffic": traffic, "kernel": f"psadam_step_kernel ({head})",
+                         "frac_of_8tbs_nominal": round(r["achieved_gbs"] / 8000.0, 4)},
+            "modes": {m: {"gparams_per_s": round(x["gparams_per_s"], 3), "achieved_gbs": round(x["achieved_gbs"], 1),
+                          "frac_of_measured_peak": round(x["achieved_gbs"] / peak, 4),
+                          "bytes_per_param": round(x["bytes_per_step"] / sum(w.sizes), 4),
+                          "median_ms": round(x["median_ms"], 5)} for m, x in results.items()},
+            "cpu_baseline": cpu,
+            "e2e": r.get("e2e"),
+            "gpu_launches": sum(x["launches"] for x in results.values()),
+            "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

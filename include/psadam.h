@@ -1,0 +1,157 @@
+/*
+ * psadam.h — C ABI of libpsadam.so: the fused AdamW parameter update with compressed
+ * moment state, for sm_103a (GB300).
+ *
+ * One call performs one optimizer step over a multi-tensor list of fp32 parameters,
+ * in place, with the moments stored in one of three forms:
+ *   adam_step_fp32   fp32 m and v                                (28 bytes moved / param)
+ *   adam_step_bf16m  bf16 m and v, round to nearest even         (20 bytes / param)
+ *   adam_step_q8     8-bit block-wise codes + fp32 block scales  (16 bytes / param + scales)
+ * (byte counts for fp32 grads; bf16 grads move 2 bytes less.)
+ *
+ * Sources of the method:
+ *   - AiDotNet PR #814 "feat: add 8-bit Adam optimizer for memory efficiency":
+ *     block-wise quantization with block size 2048, signed codes for m and unsigned
+ *     codes for v, scales recomputed every step ("dynamic quantization"),
+ *     QuantizationPercentile (default 99.9, range 0..100) for outlier-aware scaling,
+ *     optional stochastic rounding; its sequence diagram fixes the step order:
+ *     dequantize m and v, Adam update with bias correction, quantize m, quantize v.
+ *   - AiDotNet PR #1745 "perf(training): make BF16-Adam fused-compatible (proper bf16
+ *     moment kernel, not a gate)": the fused Adam/AdamW kernel over half-size bf16 m/v
+ *     buffers, configured by (lr, beta1, beta2, eps, weight decay).
+ *   - Adam (Kingma & Ba, Algorithm 1) with decoupled weight decay (Loshchilov & Hutter).
+ *
+ * What one element computes (fp32, each line one IEEE rounding, no fused multiply-add):
+ *   m' = beta1*m + (1-beta1)*g
+ *   v' = beta2*v + ((1-beta2)*g)*g
+ *   p' = p*(1 - lr*wd) - (lr/bc1) * (m' / (sqrt(v')*(1/sqrt(bc2)) + eps))
+ * with bc1 = 1 - beta1^step and bc2 = 1 - beta2^step; the per-step constants
+ * (1-beta1), (1-beta2), 1 - lr*wd, lr/bc1 and 1/sqrt(bc2) are formed in double on the
+ * host and rounded once to fp32. bf16 moments are widened exactly before and rounded to
+ * nearest even after. 8-bit moments are decoded as code*scale, the update uses the
+ * unquantized m', v', and each 2048-element block is then re-encoded:
+ *   X_m = k-th largest |m'| of the block, X_v = k-th largest v' (k = 1 for absmax)
+ *   s_m = X_m / 127, s_v = X_v / 255  (if X = 0 the block's maximum is used instead)
+ *   code = clamp(round(x / s), -127..127 for m, 0..255 for v); s = 0 gives code 0
+ *   round = nearest even, or floor(x/s + u) with u in [0,1) from Philox4x32-10
+ * where k = n - ceil(percentile * n / 100) + 1 among the block's n valid elements
+ * (nearest-rank percentile, evaluated in double on the host).
+ *
+ * Conventions common to every entry point:
+ *   - All arrays named "device" are device pointers; the host arrays that list them
+ *     (and numel) are read during the call only. The caller owns every buffer.
+ *   - Every device base pointer must be 16-byte aligned (PSADAM_ERR_MISALIGNED).
+ *   - numel[i] >= 0; a tensor with numel 0 is skipped and its pointers may be NULL.
+ *     n_tensors == 0 is a no-op.
+ *   - Each tensor is split into consecutive 2048-element blocks; the last block may be
+ *     partial. Scale arrays hold ceil(numel/2048) fp32 entries per tensor.
+ *   - step is the 1-based index of the step being taken (the caller increments it).
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default stream) and
+ *     the call returns without synchronizing. Buffers must not alias one another.
+ *   - Arguments are validated before anything is launched: on any error nothing has
+ *     been written. PSADAM_ERR_CUDA means a launch failed; psadam_last_cuda_error()
+ *     returns the cudaError_t value.
+ *   - The library allocates no device memory: tensor metadata travels as kernel
+ *     parameters; lists longer than one launch can carry are split into several launches.
+ */
+#ifndef PSADAM_H
+#define PSADAM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    PSADAM_OK = 0,
+    PSADAM_ERR_INVALID_ARG = 1, /* NULL pointer, negative size, step < 1, bad hyper-parameter */
+    PSADAM_ERR_MISALIGNED = 2,  /* a device base pointer is not 16-byte aligned */
+    PSADAM_ERR_UNSUPPORTED = 3, /* block size other than 2048, or a percentile rank above 16 */
+    PSADAM_ERR_CUDA = 4         /* a kernel launch failed (see psadam_last_cuda_error) */
+} psadam_status;
+
+typedef enum { PSADAM_GRAD_F32 = 0, PSADAM_GRAD_BF16 = 1 } psadam_grad_dtype;
+
+/* Hyper-parameters (PR #1745's fused config: lr, beta1, beta2, eps, weight decay).
+ * Requirements: 0 <= beta1 < 1, 0 <= beta2 < 1, eps >= 0; all finite. */
+typedef struct {
+    float lr;
+    float beta1;
+    float beta2;
+    float eps;
+    float weight_decay; /* decoupled: p *= 1 - lr*weight_decay each step */
+} psadam_hparams;
+
+/* 8-bit options (PR #814's BlockSize, UseStochasticRounding, QuantizationPercentile). */
+typedef struct {
+    int32_t block_size;          /* must be 2048, else PSADAM_ERR_UNSUPPORTED */
+    int32_t stochastic_rounding; /* 0: round to nearest even; 1: Philox stochastic rounding */
+    uint64_t seed;               /* Philox key (stochastic rounding only) */
+    float percentile;            /* (0, 100]; 100 = absmax. The block's rank k must be <= 16
+                                    (percentile >= ~99.27 for full blocks), else UNSUPPORTED */
+} psadam_q8_opts;
+
+/* The parameter/gradient side of a multi-tensor list. */
+typedef struct {
+    int32_t n_tensors;
+    int32_t grad_dtype;          /* psadam_grad_dtype: fp32 or bf16 grads (widened exactly) */
+    const int64_t* numel;        /* host [n_tensors] element counts */
+    float* const* param;         /* host [n_tensors] device fp32 params, updated in place */
+    const void* const* grad;     /* host [n_tensors] device grads (float* or bf16 bits), read only */
+} psadam_list;
+
+/* One AdamW step with fp32 moments. m, v: host [n_tensors] of device float[numel],
+ * updated in place. Fresh state is all zeros. */
+int adam_step_fp32(const psadam_list* list, float* const* m, float* const* v, int64_t step,
+                   const psadam_hparams* hp, void* stream);
+
+/* One AdamW step with bf16 moments (PR #1745's half-size buffers). m, v: host
+ * [n_tensors] of device uint16_t[numel] holding bf16 bit patterns, updated in place. */
+int adam_step_bf16m(const psadam_list* list, uint16_t* const* m, uint16_t* const* v, int64_t step,
+                    const psadam_hparams* hp, void* stream);
+
+/* One AdamW step with 8-bit block-wise moments (PR #814): dequantize, update and
+ * requantize in one pass. m_code: device int8_t[numel] in [-127,127]; v_code: device
+ * uint8_t[numel]; m_scale, v_scale: device float[ceil(numel/2048)]; all updated in
+ * place. Fresh state is all zeros (codes 0, scales 0). Stochastic rounding of element e
+ * of list tensor i draws word e%4 of Philox4x32-10(counter = (e/4 low, e/4 high,
+ * step low 32 bits, 2*i + moment), key = seed), moment 0 for m and 1 for v; u is the
+ * word's top 24 bits times 2^-24. */
+int adam_step_q8(const psadam_list* list, int8_t* const* m_code, uint8_t* const* v_code,
+                 float* const* m_scale, float* const* v_scale, int64_t step,
+                 const psadam_hparams* hp, const psadam_q8_opts* q8, void* stream);
+
+/* Quantize-only (PR #814's Quantize(m), Quantize(v)): encodes fp32 m, v into codes and
+ * scales exactly as adam_step_q8 encodes m', v' (same rounding, percentile and, for
+ * stochastic rounding, the same Philox stream for `step`). For state initialisation
+ * and checks. Inputs: device float m[numel], v[numel] with v >= 0. */
+int psadam_q8_quantize(int32_t n_tensors, const int64_t* numel, const float* const* m,
+                       const float* const* v, int8_t* const* m_code, uint8_t* const* v_code,
+                       float* const* m_scale, float* const* v_scale, const psadam_q8_opts* q8,
+                       int64_t step, void* stream);
+
+/* Dequantize-only (PR #814's Dequantize): m = code*scale, v = code*scale (one fp32
+ * multiply each) into device float m[numel], v[numel]. */
+int psadam_q8_dequantize(int32_t n_tensors, const int64_t* numel, const int8_t* const* m_code,
+                         const uint8_t* const* v_code, const float* const* m_scale,
+                         const float* const* v_scale, float* const* m, float* const* v,
+                         void* stream);
+
+/* Bytes of optimizer state for a tensor of numel params (PR #814's GetMemoryUsage):
+ * mode 0 = fp32 (8*numel), 1 = bf16 (4*numel), 2 = 8-bit (2*numel + 8*ceil(numel/2048)).
+ * Returns 0 for an unknown mode or numel < 0. */
+size_t psadam_state_bytes(int32_t mode, int64_t numel);
+
+/* Static, human-readable name of a psadam_status value. */
+const char* psadam_status_string(int32_t status);
+
+/* cudaError_t of the most recent PSADAM_ERR_CUDA on the calling thread (0 if none). */
+int32_t psadam_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PSADAM_H */

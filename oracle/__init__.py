@@ -90,6 +90,7 @@ def _load() -> ctypes.CDLL:
         "orc_step_bf16m": (None, [i64, _f32p, vp, i32, _u16p, _u16p, hp, i64]),
         "orc_step_q8": (None, [i64, _f32p, vp, i32, _i8p, _u8p, _f32p, _f32p, hp, i64, q8, i32,
                                i64, i64]),
+        "orc_step_q8_block": (None, [i64, i64, _f32p, vp, i32, _i8p, _u8p, _f32p, _f32p, hp, i64, q8, i32]),
         "orc_probe_mul_add": (ctypes.c_float, [ctypes.c_float] * 3),
     }
     for name, (res, args) in sigs.items():
@@ -249,6 +250,23 @@ def step_q8(p, g, mc, vc, ms, vs, t: int, hp: HParams, q8: Q8Opts = Q8Opts(), te
     _lib.orc_step_q8(n, _ptr(p, ctypes.c_float), gp, gb, _ptr(mc, ctypes.c_int8), _ptr(vc, ctypes.c_uint8),
                      _ptr(ms, ctypes.c_float), _ptr(vs, ctypes.c_float), ctypes.byref(hp._c()), t,
                      ctypes.byref(q8._c()), tensor_idx, b0, b1)
+
+
+def step_q8_block(p, g, mc, vc, ms, vs, t: int, hp: HParams, q8: Q8Opts, tensor_idx: int, elem0: int) -> None:
+    """8-bit step of one block held in its own arrays: ``p, g, mc, vc`` are the block's
+    elements (<= 2048), ``ms, vs`` one-element scale arrays, ``elem0`` the block's first
+    element index within its tensor (it keys the stochastic-rounding stream)."""
+    n = p.size
+    assert 0 < n <= BLOCK and elem0 % BLOCK == 0
+    _check(p, np.float32, "param")
+    _check(mc, np.int8, "m_code", n)
+    _check(vc, np.uint8, "v_code", n)
+    _check(ms, np.float32, "m_scale", 1)
+    _check(vs, np.float32, "v_scale", 1)
+    gp, gb = _grad(g, n)
+    _lib.orc_step_q8_block(n, elem0, _ptr(p, ctypes.c_float), gp, gb, _ptr(mc, ctypes.c_int8),
+                           _ptr(vc, ctypes.c_uint8), _ptr(ms, ctypes.c_float), _ptr(vs, ctypes.c_float),
+                           ctypes.byref(hp._c()), t, ctypes.byref(q8._c()), tensor_idx)
 
 
 # ---------------------------------------------------------------- multi-tensor lists

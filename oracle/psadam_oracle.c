@@ -282,23 +282,32 @@ void orc_dequantize(int64_t n, const int8_t* m_code, const uint8_t* v_code,
 }
 
 /* [P814] sequence diagram, per step: Dequantize(m), Dequantize(v), Adam update with
- * bias correction, Quantize(m), Quantize(v). Blocks never interact, so the four
- * phases run block by block over the requested range. */
+ * bias correction, Quantize(m), Quantize(v). Blocks never interact, so the four phases
+ * run block by block. One block: `cnt` valid elements starting at element `elem0` of
+ * its tensor; the array pointers point at the block's first element, the scale
+ * pointers at the block's scale. */
+void orc_step_q8_block(int64_t cnt, int64_t elem0, float* p, const void* grad, int grad_bf16,
+                       int8_t* m_code, uint8_t* v_code, float* m_scale, float* v_scale,
+                       const orc_hparams* hp, int64_t t, const orc_q8opts* q, int tensor_idx) {
+    orc_scalars s = orc_make_scalars(hp, t);
+    float mf[ORC_BLOCK], vf[ORC_BLOCK];
+    for (int64_t i = 0; i < cnt; ++i) mf[i] = (float)m_code[i] * *m_scale;
+    for (int64_t i = 0; i < cnt; ++i) vf[i] = (float)v_code[i] * *v_scale;
+    for (int64_t i = 0; i < cnt; ++i) adam_element(&p[i], load_grad(grad, grad_bf16, i), &mf[i], &vf[i], &s);
+    *m_scale = orc_quantize_block(mf, cnt, 1, q, t, tensor_idx, elem0, m_code, NULL);
+    *v_scale = orc_quantize_block(vf, cnt, 0, q, t, tensor_idx, elem0, NULL, v_code);
+}
+
 void orc_step_q8(int64_t n, float* p, const void* grad, int grad_bf16, int8_t* m_code,
                  uint8_t* v_code, float* m_scale, float* v_scale, const orc_hparams* hp,
                  int64_t t, const orc_q8opts* q, int tensor_idx, int64_t block_begin,
                  int64_t block_end) {
-    orc_scalars s = orc_make_scalars(hp, t);
-    float mf[ORC_BLOCK], vf[ORC_BLOCK];
+    size_t gsize = grad_bf16 ? sizeof(uint16_t) : sizeof(float);
     for (int64_t b = block_begin; b < block_end; ++b) {
         int64_t lo = b * ORC_BLOCK;
         int64_t cnt = n - lo < ORC_BLOCK ? n - lo : ORC_BLOCK;
-        for (int64_t i = 0; i < cnt; ++i) mf[i] = (float)m_code[lo + i] * m_scale[b];
-        for (int64_t i = 0; i < cnt; ++i) vf[i] = (float)v_code[lo + i] * v_scale[b];
-        for (int64_t i = 0; i < cnt; ++i)
-            adam_element(&p[lo + i], load_grad(grad, grad_bf16, lo + i), &mf[i], &vf[i], &s);
-        m_scale[b] = orc_quantize_block(mf, cnt, 1, q, t, tensor_idx, lo, m_code + lo, NULL);
-        v_scale[b] = orc_quantize_block(vf, cnt, 0, q, t, tensor_idx, lo, NULL, v_code + lo);
+        orc_step_q8_block(cnt, lo, p + lo, (const char*)grad + (size_t)lo * gsize, grad_bf16,
+                          m_code + lo, v_code + lo, m_scale + b, v_scale + b, hp, t, q, tensor_idx);
     }
 }
 

@@ -95,6 +95,13 @@ void orc_step_q8(int64_t n, float* p, const void* grad, int grad_bf16, int8_t* m
                  int64_t t, const orc_q8opts* q, int tensor_idx, int64_t block_begin,
                  int64_t block_end);
 
+/* The same step for one block: cnt (<= ORC_BLOCK) valid elements that start at element
+ * elem0 of their tensor; array pointers point at the block's first element and the
+ * scale pointers at the block's own scale. */
+void orc_step_q8_block(int64_t cnt, int64_t elem0, float* p, const void* grad, int grad_bf16,
+                       int8_t* m_code, uint8_t* v_code, float* m_scale, float* v_scale,
+                       const orc_hparams* hp, int64_t t, const orc_q8opts* q, int tensor_idx);
+
 /* Build-flag probe: returns a*b + c with two roundings. A build that let the
  * compiler contract this into one fused multiply-add would return the fused value. */
 float orc_probe_mul_add(float a, float b, float c);

@@ -1,0 +1,269 @@
+"""precision_state_adam_gb300 — fused AdamW with compressed moment state on GB300.
+
+A thin ctypes binding over libpsadam.so (the C ABI in include/psadam.h). Every function
+here only marshals torch tensors into pointer tables and calls the library; the
+arithmetic runs in the library's sm_103a kernels. There is no CPU fallback: importing
+this package fails if the library has not been built.
+
+Entry points (same names as the C ABI):
+    adam_step_fp32(params, grads, m, v, step, ...)              fp32 moments
+    adam_step_bf16m(params, grads, m, v, step, ...)             bf16 moments (torch.bfloat16 tensors)
+    adam_step_q8(params, grads, m_code, v_code, m_scale, v_scale, step, ...)
+    q8_quantize / q8_dequantize                                 8-bit state conversion
+    state_bytes(mode, numel)                                    optimizer-state footprint
+and helpers to allocate fresh (zero) state with the right dtypes and shapes.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Sequence
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libpsadam.so")
+BLOCK = 2048
+MAX_PERCENTILE_RANK = 16
+
+OK, ERR_INVALID_ARG, ERR_MISALIGNED, ERR_UNSUPPORTED, ERR_CUDA = range(5)
+GRAD_F32, GRAD_BF16 = 0, 1
+MODES = {"fp32": 0, "bf16m": 1, "q8": 2}
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"{LIB_PATH} is missing: build it with `python -c 'import __graft_entry__ as g; g.build()'` "
+        "(or `python precision_state_adam_gb300/build.py`). There is no CPU fallback.")
+
+
+class _HParams(ctypes.Structure):
+    _fields_ = [("lr", ctypes.c_float), ("beta1", ctypes.c_float), ("beta2", ctypes.c_float),
+                ("eps", ctypes.c_float), ("weight_decay", ctypes.c_float)]
+
+
+class _Q8Opts(ctypes.Structure):
+    _fields_ = [("block_size", ctypes.c_int32), ("stochastic_rounding", ctypes.c_int32),
+                ("seed", ctypes.c_uint64), ("percentile", ctypes.c_float)]
+
+
+class _List(ctypes.Structure):
+    _fields_ = [("n_tensors", ctypes.c_int32), ("grad_dtype", ctypes.c_int32),
+                ("numel", ctypes.POINTER(ctypes.c_int64)), ("param", ctypes.POINTER(ctypes.c_void_p)),
+                ("grad", ctypes.POINTER(ctypes.c_void_p))]
+
+
+_lib = ctypes.CDLL(LIB_PATH)
+_vp = ctypes.c_void_p
+_PP = ctypes.POINTER(ctypes.c_void_p)
+_I64P = ctypes.POINTER(ctypes.c_int64)
+_SIGS = {
+    "adam_step_fp32": [ctypes.POINTER(_List), _PP, _PP, ctypes.c_int64, ctypes.POINTER(_HParams), _vp],
+    "adam_step_bf16m": [ctypes.POINTER(_List), _PP, _PP, ctypes.c_int64, ctypes.POINTER(_HParams), _vp],
+    "adam_step_q8": [ctypes.POINTER(_List), _PP, _PP, _PP, _PP, ctypes.c_int64, ctypes.POINTER(_HParams),
+                     ctypes.POINTER(_Q8Opts), _vp],
+    "psadam_q8_quantize": [ctypes.c_int32, _I64P, _PP, _PP, _PP, _PP, _PP, _PP, ctypes.POINTER(_Q8Opts),
+                           ctypes.c_int64, _vp],
+    "psadam_q8_dequantize": [ctypes.c_int32, _I64P, _PP, _PP, _PP, _PP, _PP, _PP, _vp],
+}
+for _name, _args in _SIGS.items():
+    getattr(_lib, _name).argtypes = _args
+    getattr(_lib, _name).restype = ctypes.c_int
+_lib.psadam_state_bytes.argtypes = [ctypes.c_int32, ctypes.c_int64]
+_lib.psadam_state_bytes.restype = ctypes.c_size_t
+_lib.psadam_status_string.argtypes = [ctypes.c_int32]
+_lib.psadam_status_string.restype = ctypes.c_char_p
+_lib.psadam_last_cuda_error.argtypes = []
+_lib.psadam_last_cuda_error.restype = ctypes.c_int32
+
+
+class PSAdamError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        msg = f"{where}: {status_string(status)}"
+        if status == ERR_CUDA:
+            msg += f" (cudaError {_lib.psadam_last_cuda_error()})"
+        super().__init__(msg)
+
+
+def status_string(status: int) -> str:
+    return _lib.psadam_status_string(status).decode()
+
+
+def state_bytes(mode: str | int, numel: int) -> int:
+    return int(_lib.psadam_state_bytes(MODES.get(mode, mode) if isinstance(mode, str) else mode, numel))
+
+
+def n_blocks(numel: int) -> int:
+    return (numel + BLOCK - 1) // BLOCK
+
+
+# ------------------------------------------------------------------ marshalling
+def _ptrs(ts: Sequence[torch.Tensor | None]):
+    arr = (ctypes.c_void_p * max(len(ts), 1))()
+    for i, t in enumerate(ts):
+        arr[i] = None if t is None or t.numel() == 0 else t.data_ptr()
+    return arr
+
+
+def _numels(ts: Sequence[torch.Tensor]):
+    arr = (ctypes.c_int64 * max(len(ts), 1))()
+    for i, t in enumerate(ts):
+        arr[i] = t.numel()
+    return arr
+
+
+def _stream_handle(stream, ts) -> int | None:
+    if stream is None:
+        dev = next((t.device for t in ts if t is not None and t.is_cuda), None)
+        stream = torch.cuda.current_stream(dev) if dev is not None else None
+    if stream is None:
+        return None
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _check_layout(name: str, ts, dtype, like=None, numel_fn=None) -> None:
+    for i, t in enumerate(ts):
+        if t.dtype != dtype:
+            raise TypeError(f"{name}[{i}]: expected {dtype}, got {t.dtype}")
+        if not t.is_cuda:
+            raise TypeError(f"{name}[{i}]: must be a CUDA tensor")
+        if not t.is_contiguous():
+            raise ValueError(f"{name}[{i}]: must be contiguous")
+        if like is not None:
+            want = numel_fn(like[i].numel()) if numel_fn else like[i].numel()
+            if t.numel() != want:
+                raise ValueError(f"{name}[{i}]: expected {want} elements, got {t.numel()}")
+
+
+def _hp(lr, beta1, beta2, eps, weight_decay) -> _HParams:
+    return _HParams(lr, beta1, beta2, eps, weight_decay)
+
+
+def _list(params, grads):
+    if len(params) != len(grads):
+        raise ValueError("params and grads differ in length")
+    _check_layout("params", params, torch.float32)
+    gdt = grads[0].dtype if grads else torch.float32
+    if gdt not in (torch.float32, torch.bfloat16):
+        raise TypeError("grads must be float32 or bfloat16")
+    _check_layout("grads", grads, gdt, params)
+    keep = (_numels(params), _ptrs(params), _ptrs(grads))
+    lst = _List(len(params), GRAD_BF16 if gdt == torch.bfloat16 else GRAD_F32, keep[0],
+                ctypes.cast(keep[1], _PP), ctypes.cast(keep[2], _PP))
+    return lst, keep
+
+
+def _raise(status: int, where: str) -> None:
+    if status != OK:
+        raise PSAdamError(status, where)
+
+
+# ------------------------------------------------------------------ steps
+def adam_step_fp32(params, grads, m, v, step: int, lr: float = 1e-3, beta1: float = 0.9, beta2: float = 0.999,
+                   eps: float = 1e-8, weight_decay: float = 0.0, stream=None) -> None:
+    """One AdamW step with fp32 moments, in place, enqueued on ``stream`` (default: current)."""
+    lst, keep = _list(params, grads)
+    _check_layout("m", m, torch.float32, params)
+    _check_layout("v", v, torch.float32, params)
+    mp, vp = _ptrs(m), _ptrs(v)
+    st = _lib.adam_step_fp32(ctypes.byref(lst), ctypes.cast(mp, _PP), ctypes.cast(vp, _PP), step,
+                             ctypes.byref(_hp(lr, beta1, beta2, eps, weight_decay)), _stream_handle(stream, params))
+    _raise(st, "adam_step_fp32")
+
+
+def adam_step_bf16m(params, grads, m, v, step: int, lr: float = 1e-3, beta1: float = 0.9, beta2: float = 0.999,
+                    eps: float = 1e-8, weight_decay: float = 0.0, stream=None) -> None:
+    """One AdamW step with bf16 moments (torch.bfloat16 tensors), in place."""
+    lst, keep = _list(params, grads)
+    _check_layout("m", m, torch.bfloat16, params)
+    _check_layout("v", v, torch.bfloat16, params)
+    mp, vp = _ptrs(m), _ptrs(v)
+    st = _lib.adam_step_bf16m(ctypes.byref(lst), ctypes.cast(mp, _PP), ctypes.cast(vp, _PP), step,
+                              ctypes.byref(_hp(lr, beta1, beta2, eps, weight_decay)), _stream_handle(stream, params))
+    _raise(st, "adam_step_bf16m")
+
+
+def _q8(stochastic_rounding: bool, seed: int, percentile: float, block_size: int) -> _Q8Opts:
+    return _Q8Opts(block_size, int(bool(stochastic_rounding)), seed, percentile)
+
+
+def adam_step_q8(params, grads, m_code, v_code, m_scale, v_scale, step: int, lr: float = 1e-3, beta1: float = 0.9,
+                 beta2: float = 0.999, eps: float = 1e-8, weight_decay: float = 0.0, stochastic_rounding: bool = False,
+                 seed: int = 42, percentile: float = 100.0, block_size: int = BLOCK, stream=None) -> None:
+    """One AdamW step with 8-bit block-wise moments (int8 m codes, uint8 v codes, fp32
+    per-block scales), dequantize-update-requantize in one pass, in place."""
+    lst, keep = _list(params, grads)
+    _check_layout("m_code", m_code, torch.int8, params)
+    _check_layout("v_code", v_code, torch.uint8, params)
+    _check_layout("m_scale", m_scale, torch.float32, params, n_blocks)
+    _check_layout("v_scale", v_scale, torch.float32, params, n_blocks)
+    ptrs = [_ptrs(x) for x in (m_code, v_code, m_scale, v_scale)]
+    st = _lib.adam_step_q8(ctypes.byref(lst), *[ctypes.cast(p, _PP) for p in ptrs], step,
+                           ctypes.byref(_hp(lr, beta1, beta2, eps, weight_decay)),
+                           ctypes.byref(_q8(stochastic_rounding, seed, percentile, block_size)),
+                           _stream_handle(stream, params))
+    _raise(st, "adam_step_q8")
+
+
+def q8_quantize(m, v, m_code, v_code, m_scale, v_scale, step: int = 1, stochastic_rounding: bool = False,
+                seed: int = 42, percentile: float = 100.0, block_size: int = BLOCK, stream=None) -> None:
+    """Encode fp32 moments into 8-bit codes and block scales (as the step encodes m', v')."""
+    _check_layout("m", m, torch.float32)
+    _check_layout("v", v, torch.float32, m)
+    _check_layout("m_code", m_code, torch.int8, m)
+    _check_layout("v_code", v_code, torch.uint8, m)
+    _check_layout("m_scale", m_scale, torch.float32, m, n_blocks)
+    _check_layout("v_scale", v_scale, torch.float32, m, n_blocks)
+    ptrs = [_ptrs(x) for x in (m, v, m_code, v_code, m_scale, v_scale)]
+    st = _lib.psadam_q8_quantize(len(m), _numels(m), *[ctypes.cast(p, _PP) for p in ptrs],
+                                 ctypes.byref(_q8(stochastic_rounding, seed, percentile, block_size)), step,
+                                 _stream_handle(stream, m))
+    _raise(st, "psadam_q8_quantize")
+
+
+def q8_dequantize(m_code, v_code, m_scale, v_scale, m, v, stream=None) -> None:
+    """Decode 8-bit codes and block scales into fp32 moments (code * scale)."""
+    _check_layout("m_code", m_code, torch.int8)
+    _check_layout("v_code", v_code, torch.uint8, m_code)
+    _check_layout("m_scale", m_scale, torch.float32, m_code, n_blocks)
+    _check_layout("v_scale", v_scale, torch.float32, m_code, n_blocks)
+    _check_layout("m", m, torch.float32, m_code)
+    _check_layout("v", v, torch.float32, m_code)
+    ptrs = [_ptrs(x) for x in (m_code, v_code, m_scale, v_scale, m, v)]
+    st = _lib.psadam_q8_dequantize(len(m_code), _numels(m_code), *[ctypes.cast(p, _PP) for p in ptrs],
+                                   _stream_handle(stream, m))
+    _raise(st, "psadam_q8_dequantize")
+
+
+# ------------------------------------------------------------------ state allocation (caller side)
+def zeros_state(params, mode: str):
+    """Fresh (all-zero) optimizer state for ``params`` in moment mode ``mode``.
+    fp32/bf16m: (m list, v list); q8: (m_code, v_code, m_scale, v_scale) lists."""
+    if mode == "fp32":
+        return [torch.zeros_like(p) for p in params], [torch.zeros_like(p) for p in params]
+    if mode == "bf16m":
+        z = lambda p: torch.zeros(p.numel(), dtype=torch.bfloat16, device=p.device)
+        return [z(p) for p in params], [z(p) for p in params]
+    if mode == "q8":
+        return ([torch.zeros(p.numel(), dtype=torch.int8, device=p.device) for p in params],
+                [torch.zeros(p.numel(), dtype=torch.uint8, device=p.device) for p in params],
+                [torch.zeros(n_blocks(p.numel()), dtype=torch.float32, device=p.device) for p in params],
+                [torch.zeros(n_blocks(p.numel()), dtype=torch.float32, device=p.device) for p in params])
+    raise ValueError(f"unknown moment mode {mode!r}")
+
+
+def adam_step(mode: str, params, grads, state, step: int, **kw) -> None:
+    """Dispatch by moment mode name: ``state`` as returned by :func:`zeros_state`."""
+    if mode == "fp32":
+        adam_step_fp32(params, grads, *state, step, **kw)
+    elif mode == "bf16m":
+        adam_step_bf16m(params, grads, *state, step, **kw)
+    elif mode == "q8":
+        adam_step_q8(params, grads, *state, step, **kw)
+    else:
+        raise ValueError(f"unknown moment mode {mode!r}")
+
+
+def cdll() -> ctypes.CDLL:
+    """The loaded libpsadam.so handle (for ABI-level tests)."""
+    return _lib

@@ -1,0 +1,318 @@
+// psadam_api.cu — the C ABI declared in include/psadam.h: argument validation, the
+// per-step constants, tensor-list packing into launch-parameter blocks, and dispatch to
+// the kernel instantiations. No device memory is allocated here.
+#include <climits>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <vector>
+
+#include "psadam.h"
+#include "psadam_internal.h"
+
+using namespace psadam;
+
+namespace {
+
+thread_local int32_t g_last_cuda_error = 0;
+
+// Largest tensor whose block count fits a grid dimension.
+constexpr long long kMaxNumel = (long long)INT_MAX * kBlock;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool finite(float x) { return std::isfinite(x); }
+
+struct Entry {
+  float* p;
+  const void* g;
+  void* m;
+  void* v;
+  float* ms;
+  float* vs;
+  long long numel;
+  int list_idx;
+};
+
+int check_hparams(const psadam_hparams* hp, int64_t step) {
+  if (!hp || step < 1) return PSADAM_ERR_INVALID_ARG;
+  if (!finite(hp->lr) || !finite(hp->beta1) || !finite(hp->beta2) || !finite(hp->eps) ||
+      !finite(hp->weight_decay))
+    return PSADAM_ERR_INVALID_ARG;
+  if (hp->beta1 < 0.f || hp->beta1 >= 1.f || hp->beta2 < 0.f || hp->beta2 >= 1.f || hp->eps < 0.f)
+    return PSADAM_ERR_INVALID_ARG;
+  return PSADAM_OK;
+}
+
+int check_q8(const psadam_q8_opts* q) {
+  if (!q) return PSADAM_ERR_INVALID_ARG;
+  if (q->block_size != kBlock) return PSADAM_ERR_UNSUPPORTED;
+  if (q->stochastic_rounding != 0 && q->stochastic_rounding != 1) return PSADAM_ERR_INVALID_ARG;
+  if (!finite(q->percentile) || !(q->percentile > 0.f) || q->percentile > 100.f) return PSADAM_ERR_INVALID_ARG;
+  return PSADAM_OK;
+}
+
+// Per-step constants: bias corrections 1 - beta^t from pow() in double (the 8-bit Adam
+// PR's UpdateParameters forms them with Math.Pow on doubles), each constant rounded
+// once to fp32.
+StepConsts make_consts(const psadam_hparams& hp, int64_t t) {
+  const double lr = hp.lr, b1 = hp.beta1, b2 = hp.beta2, wd = hp.weight_decay;
+  const double bc1 = 1.0 - std::pow(b1, (double)t);
+  const double bc2 = 1.0 - std::pow(b2, (double)t);
+  StepConsts c;
+  c.b1 = hp.beta1;
+  c.omb1 = (float)(1.0 - b1);
+  c.b2 = hp.beta2;
+  c.omb2 = (float)(1.0 - b2);
+  c.decay = (float)(1.0 - lr * wd);
+  c.step_size = (float)(lr / bc1);
+  c.inv_sqrt_bc2 = (float)(1.0 / std::sqrt(bc2));
+  c.eps = hp.eps;
+  return c;
+}
+
+// Nearest-rank percentile as a position from the top: k = n - ceil(pct*n/100) + 1.
+int percentile_rank(float pct, long long n) {
+  long long from_bottom = (long long)std::ceil((double)pct * (double)n / 100.0);
+  long long k = n - from_bottom + 1;
+  if (k < 1) k = 1;
+  if (k > n) k = n;
+  return (int)k;
+}
+
+long long n_blocks(long long n) { return (n + kBlock - 1) / kBlock; }
+int last_block_len(long long n) { return (int)(n - (n_blocks(n) - 1) * kBlock); }
+
+// Validate one tensor's pointers. `ptrs` lists the ones that must be present.
+int check_tensor(long long numel, std::initializer_list<const void*> ptrs) {
+  if (numel < 0) return PSADAM_ERR_INVALID_ARG;
+  if (numel == 0) return PSADAM_OK;
+  if (numel > kMaxNumel) return PSADAM_ERR_UNSUPPORTED;
+  for (const void* p : ptrs)
+    if (!p) return PSADAM_ERR_INVALID_ARG;
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return PSADAM_ERR_MISALIGNED;
+  return PSADAM_OK;
+}
+
+// Highest percentile rank any block of the list needs.
+int max_rank(const std::vector<Entry>& es, float pct) {
+  int k = 1;
+  for (const Entry& e : es) {
+    if (e.numel >= kBlock) k = std::max(k, percentile_rank(pct, kBlock));
+    k = std::max(k, percentile_rank(pct, last_block_len(e.numel)));
+  }
+  return k;
+}
+
+template <int CAP>
+using Launcher = cudaError_t (*)(const LaunchArgs<CAP>&, cudaStream_t);
+
+// Pack the list into as few launches as fit and run `fn` on each.
+template <int CAP>
+int run_launches(const std::vector<Entry>& es, const StepConsts& c, uint64_t seed, int64_t step, float pct,
+                 Launcher<CAP> fn, cudaStream_t stream) {
+  static thread_local LaunchArgs<CAP> a;  // ~32 KB: keep it off the stack
+  std::memset(&a, 0, sizeof a);
+  a.c = c;
+  a.seed_lo = (uint32_t)(seed & 0xFFFFFFFFu);
+  a.seed_hi = (uint32_t)(seed >> 32);
+  a.step_lo = (uint32_t)step;
+  a.k_full = percentile_rank(pct, kBlock);
+  size_t i = 0;
+  while (i < es.size()) {
+    int nt = 0;
+    long long blocks = 0;
+    while (i < es.size() && nt < CAP) {
+      const long long nb = n_blocks(es[i].numel);
+      if (blocks + nb > INT_MAX) break;
+      TensorRef& t = a.t[nt++];
+      t.p = es[i].p;
+      t.g = es[i].g;
+      t.m = es[i].m;
+      t.v = es[i].v;
+      t.ms = es[i].ms;
+      t.vs = es[i].vs;
+      t.numel = es[i].numel;
+      t.block_begin = (int)blocks;
+      t.k_last = percentile_rank(pct, last_block_len(es[i].numel));
+      t.list_idx = es[i].list_idx;
+      blocks += nb;
+      ++i;
+    }
+    a.n_tensors = nt;
+    a.total_blocks = (int)blocks;
+    const cudaError_t err = fn(a, stream);
+    if (err != cudaSuccess) {
+      g_last_cuda_error = (int32_t)err;
+      return PSADAM_ERR_CUDA;
+    }
+  }
+  return PSADAM_OK;
+}
+
+#define PSADAM_STEP_FN(MODE, GB, SR, K, CAP) &launch_step<MODE, GB, SR, K, CAP>
+
+template <int CAP>
+Launcher<CAP> pick_step(int mode, bool gb, bool sr, int K) {
+  if (mode == kModeF32) return gb ? PSADAM_STEP_FN(kModeF32, true, false, 1, CAP) : PSADAM_STEP_FN(kModeF32, false, false, 1, CAP);
+  if (mode == kModeBF16) return gb ? PSADAM_STEP_FN(kModeBF16, true, false, 1, CAP) : PSADAM_STEP_FN(kModeBF16, false, false, 1, CAP);
+#define PSADAM_PICK_K(GB, SR)                                         \
+  if (K == 1) return PSADAM_STEP_FN(kModeQ8, GB, SR, 1, CAP);         \
+  if (K == 4) return PSADAM_STEP_FN(kModeQ8, GB, SR, 4, CAP);         \
+  return PSADAM_STEP_FN(kModeQ8, GB, SR, 16, CAP);
+  if (gb) {
+    if (sr) { PSADAM_PICK_K(true, true) } else { PSADAM_PICK_K(true, false) }
+  } else {
+    if (sr) { PSADAM_PICK_K(false, true) } else { PSADAM_PICK_K(false, false) }
+  }
+#undef PSADAM_PICK_K
+}
+
+template <int CAP>
+Launcher<CAP> pick_quantize(bool sr, int K) {
+  if (sr) return K == 1 ? &launch_quantize<true, 1, CAP> : (K == 4 ? &launch_quantize<true, 4, CAP> : &launch_quantize<true, 16, CAP>);
+  return K == 1 ? &launch_quantize<false, 1, CAP> : (K == 4 ? &launch_quantize<false, 4, CAP> : &launch_quantize<false, 16, CAP>);
+}
+
+// Dispatch on list length: short lists use the small parameter block.
+int dispatch(const std::vector<Entry>& es, const StepConsts& c, uint64_t seed, int64_t step, float pct,
+             Launcher<kCapSmall> small, Launcher<kCapLarge> large, cudaStream_t stream) {
+  if (es.empty()) return PSADAM_OK;
+  if (es.size() <= (size_t)kCapSmall) return run_launches<kCapSmall>(es, c, seed, step, pct, small, stream);
+  return run_launches<kCapLarge>(es, c, seed, step, pct, large, stream);
+}
+
+// Shared front half of the three step entry points.
+int collect_list(const psadam_list* list, const void* const* m, const void* const* v, const float* const* ms,
+                 const float* const* vs, bool q8, std::vector<Entry>& out) {
+  if (!list || list->n_tensors < 0) return PSADAM_ERR_INVALID_ARG;
+  if (list->n_tensors == 0) return PSADAM_OK;
+  if (list->grad_dtype != PSADAM_GRAD_F32 && list->grad_dtype != PSADAM_GRAD_BF16) return PSADAM_ERR_INVALID_ARG;
+  if (!list->numel || !list->param || !list->grad || !m || !v || (q8 && (!ms || !vs)))
+    return PSADAM_ERR_INVALID_ARG;
+  out.reserve(list->n_tensors);
+  for (int i = 0; i < list->n_tensors; ++i) {
+    const long long n = list->numel[i];
+    const int st = q8 ? check_tensor(n, {list->param[i], list->grad[i], m[i], v[i], ms[i], vs[i]})
+                      : check_tensor(n, {list->param[i], list->grad[i], m[i], v[i]});
+    if (st != PSADAM_OK) return st;
+    if (n == 0) continue;
+    out.push_back(Entry{list->param[i], list->grad[i], const_cast<void*>(m[i]), const_cast<void*>(v[i]),
+                        q8 ? const_cast<float*>(ms[i]) : nullptr, q8 ? const_cast<float*>(vs[i]) : nullptr, n, i});
+  }
+  return PSADAM_OK;
+}
+
+int step_common(int mode, const psadam_list* list, const void* const* m, const void* const* v,
+                const float* const* ms, const float* const* vs, int64_t step, const psadam_hparams* hp,
+                const psadam_q8_opts* q8, void* stream) {
+  if (!list || list->n_tensors < 0) return PSADAM_ERR_INVALID_ARG;
+  if (list->n_tensors == 0) return PSADAM_OK;
+  int st = check_hparams(hp, step);
+  if (st != PSADAM_OK) return st;
+  if (mode == kModeQ8 && (st = check_q8(q8)) != PSADAM_OK) return st;
+  std::vector<Entry> es;
+  if ((st = collect_list(list, m, v, ms, vs, mode == kModeQ8, es)) != PSADAM_OK) return st;
+  const float pct = mode == kModeQ8 ? q8->percentile : 100.f;
+  const bool sr = mode == kModeQ8 && q8->stochastic_rounding;
+  const uint64_t seed = mode == kModeQ8 ? q8->seed : 0;
+  const int kmax = max_rank(es, pct);
+  if (kmax > kMaxRank) return PSADAM_ERR_UNSUPPORTED;
+  const int K = rank_template(kmax);
+  const bool gb = list->grad_dtype == PSADAM_GRAD_BF16;
+  const StepConsts c = make_consts(*hp, step);
+  return dispatch(es, c, seed, step, pct, pick_step<kCapSmall>(mode, gb, sr, K), pick_step<kCapLarge>(mode, gb, sr, K),
+                  static_cast<cudaStream_t>(stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+int adam_step_fp32(const psadam_list* list, float* const* m, float* const* v, int64_t step,
+                   const psadam_hparams* hp, void* stream) {
+  return step_common(kModeF32, list, reinterpret_cast<const void* const*>(m), reinterpret_cast<const void* const*>(v),
+                     nullptr, nullptr, step, hp, nullptr, stream);
+}
+
+int adam_step_bf16m(const psadam_list* list, uint16_t* const* m, uint16_t* const* v, int64_t step,
+                    const psadam_hparams* hp, void* stream) {
+  return step_common(kModeBF16, list, reinterpret_cast<const void* const*>(m), reinterpret_cast<const void* const*>(v),
+                     nullptr, nullptr, step, hp, nullptr, stream);
+}
+
+int adam_step_q8(const psadam_list* list, int8_t* const* m_code, uint8_t* const* v_code, float* const* m_scale,
+                 float* const* v_scale, int64_t step, const psadam_hparams* hp, const psadam_q8_opts* q8,
+                 void* stream) {
+  return step_common(kModeQ8, list, reinterpret_cast<const void* const*>(m_code),
+                     reinterpret_cast<const void* const*>(v_code), m_scale, v_scale, step, hp, q8, stream);
+}
+
+int psadam_q8_quantize(int32_t n_tensors, const int64_t* numel, const float* const* m, const float* const* v,
+                       int8_t* const* m_code, uint8_t* const* v_code, float* const* m_scale, float* const* v_scale,
+                       const psadam_q8_opts* q8, int64_t step, void* stream) {
+  if (n_tensors < 0) return PSADAM_ERR_INVALID_ARG;
+  if (n_tensors == 0) return PSADAM_OK;
+  int st = check_q8(q8);
+  if (st != PSADAM_OK) return st;
+  if (!numel || !m || !v || !m_code || !v_code || !m_scale || !v_scale || step < 1) return PSADAM_ERR_INVALID_ARG;
+  std::vector<Entry> es;
+  for (int i = 0; i < n_tensors; ++i) {
+    if ((st = check_tensor(numel[i], {m[i], v[i], m_code[i], v_code[i], m_scale[i], v_scale[i]})) != PSADAM_OK)
+      return st;
+    if (numel[i] == 0) continue;
+    // codes travel in the p (m codes) and g (v codes) slots
+    es.push_back(Entry{reinterpret_cast<float*>(m_code[i]), v_code[i], const_cast<float*>(m[i]),
+                       const_cast<float*>(v[i]), m_scale[i], v_scale[i], numel[i], i});
+  }
+  const int kmax = max_rank(es, q8->percentile);
+  if (kmax > kMaxRank) return PSADAM_ERR_UNSUPPORTED;
+  const int K = rank_template(kmax);
+  const bool sr = q8->stochastic_rounding != 0;
+  return dispatch(es, StepConsts{}, q8->seed, step, q8->percentile, pick_quantize<kCapSmall>(sr, K),
+                  pick_quantize<kCapLarge>(sr, K), static_cast<cudaStream_t>(stream));
+}
+
+int psadam_q8_dequantize(int32_t n_tensors, const int64_t* numel, const int8_t* const* m_code,
+                         const uint8_t* const* v_code, const float* const* m_scale, const float* const* v_scale,
+                         float* const* m, float* const* v, void* stream) {
+  if (n_tensors < 0) return PSADAM_ERR_INVALID_ARG;
+  if (n_tensors == 0) return PSADAM_OK;
+  if (!numel || !m || !v || !m_code || !v_code || !m_scale || !v_scale) return PSADAM_ERR_INVALID_ARG;
+  std::vector<Entry> es;
+  for (int i = 0; i < n_tensors; ++i) {
+    const int st = check_tensor(numel[i], {m[i], v[i], m_code[i], v_code[i], m_scale[i], v_scale[i]});
+    if (st != PSADAM_OK) return st;
+    if (numel[i] == 0) continue;
+    es.push_back(Entry{reinterpret_cast<float*>(const_cast<int8_t*>(m_code[i])), v_code[i], m[i], v[i],
+                       const_cast<float*>(m_scale[i]), const_cast<float*>(v_scale[i]), numel[i], i});
+  }
+  return dispatch(es, StepConsts{}, 0, 1, 100.f, &launch_dequantize<kCapSmall>, &launch_dequantize<kCapLarge>,
+                  static_cast<cudaStream_t>(stream));
+}
+
+size_t psadam_state_bytes(int32_t mode, int64_t numel) {
+  if (numel < 0) return 0;
+  const size_t n = (size_t)numel;
+  switch (mode) {
+    case 0: return 8 * n;
+    case 1: return 4 * n;
+    case 2: return 2 * n + 8 * (size_t)n_blocks(numel);
+    default: return 0;
+  }
+}
+
+const char* psadam_status_string(int32_t status) {
+  switch (status) {
+    case PSADAM_OK: return "PSADAM_OK";
+    case PSADAM_ERR_INVALID_ARG: return "PSADAM_ERR_INVALID_ARG";
+    case PSADAM_ERR_MISALIGNED: return "PSADAM_ERR_MISALIGNED";
+    case PSADAM_ERR_UNSUPPORTED: return "PSADAM_ERR_UNSUPPORTED";
+    case PSADAM_ERR_CUDA: return "PSADAM_ERR_CUDA";
+    default: return "PSADAM_ERR_UNKNOWN";
+  }
+}
+
+int32_t psadam_last_cuda_error(void) { return g_last_cuda_error; }
+
+}  // extern "C"

@@ -1,0 +1,71 @@
+// psadam_internal.h — launch-argument layout shared by the host API and the kernel
+// translation units of libpsadam.so (not installed; the public ABI is include/psadam.h).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace psadam {
+
+constexpr int kBlock = 2048;   // quantization block = elements handled by one CTA
+constexpr int kThreads = 256;  // threads per CTA
+constexpr int kVec = 4;        // consecutive elements per thread per group (one 16-byte fp32 vector)
+constexpr int kGroups = kBlock / (kThreads * kVec);  // 2 groups of 4 elements per thread
+constexpr int kWarps = kThreads / 32;
+
+// Tensor-list capacities of one launch: small lists use a small kernel-parameter block,
+// long lists the largest block that stays under the 32,764-byte parameter limit.
+constexpr int kCapSmall = 8;
+constexpr int kCapLarge = 440;
+constexpr int kMaxRank = 16;  // largest percentile rank k the 8-bit kernels select
+
+enum Mode : int { kModeF32 = 0, kModeBF16 = 1, kModeQ8 = 2 };
+
+// Per-step fp32 constants (formed in double on the host, rounded once).
+struct StepConsts {
+  float b1, omb1, b2, omb2, decay, step_size, inv_sqrt_bc2, eps;
+};
+
+// One non-empty tensor of the list. For the quantize-only kernel p/g are unused and
+// m/v are the fp32 inputs; for dequantize-only m/v are the fp32 outputs and the codes
+// travel in g (m codes) and p (v codes).
+struct TensorRef {
+  float* p;
+  const void* g;
+  void* m;
+  void* v;
+  float* ms;
+  float* vs;
+  long long numel;
+  int block_begin;  // index of this tensor's first CTA within the launch
+  int k_last;       // percentile rank of the tensor's last block (may be partial)
+  int list_idx;     // position in the caller's list (stochastic-rounding stream)
+  int pad_;
+};
+
+template <int CAP>
+struct LaunchArgs {
+  StepConsts c;
+  uint32_t seed_lo, seed_hi, step_lo;
+  int k_full;       // percentile rank of a full 2048-element block
+  int n_tensors;
+  int total_blocks;
+  int pad_[2];
+  TensorRef t[CAP];
+};
+static_assert(sizeof(LaunchArgs<kCapLarge>) <= 32764, "kernel parameter block too large");
+
+// Rank templates: K = 1 (absmax), 4 or 16 (k-th largest for k <= K).
+constexpr int rank_template(int k) { return k <= 1 ? 1 : (k <= 4 ? 4 : 16); }
+
+// Launchers, explicitly instantiated in the kernel translation units.
+template <int MODE, bool GBF16, bool SR, int K, int CAP>
+cudaError_t launch_step(const LaunchArgs<CAP>& a, cudaStream_t s);
+
+template <bool SR, int K, int CAP>
+cudaError_t launch_quantize(const LaunchArgs<CAP>& a, cudaStream_t s);
+
+template <int CAP>
+cudaError_t launch_dequantize(const LaunchArgs<CAP>& a, cudaStream_t s);
+
+}  // namespace psadam

@@ -1,0 +1,115 @@
+"""Host-side checks of libpsadam.so without a GPU: the library loads, exports every
+function include/psadam.h declares, rejects bad arguments before launching anything,
+and reports the state-memory closed form (AiDotNet PR #814: 8-bit state is about 2 bytes
+per parameter plus per-block scales, ~4x less than fp32 Adam's two moments)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "psadam.h")
+
+
+@pytest.fixture(scope="module")
+def psa():
+    from precision_state_adam_gb300 import build
+    build.build()
+    import precision_state_adam_gb300 as psa
+    return psa
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b([A-Za-z_]\w*)\s*\(", text, flags=re.M)
+    return sorted({n for n in names if n not in ("if", "while", "return")})
+
+
+def test_header_declares_the_step_entry_points():
+    names = declared_functions()
+    for want in ("adam_step_fp32", "adam_step_bf16m", "adam_step_q8", "psadam_q8_quantize",
+                 "psadam_q8_dequantize", "psadam_state_bytes", "psadam_status_string"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(psa):
+    lib = ctypes.CDLL(psa.LIB_PATH)
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_library_does_not_link_the_oracle(psa):
+    data = open(psa.LIB_PATH, "rb").read()
+    assert b"orc_step" not in data and b"liboracle" not in data
+
+
+def test_state_bytes_closed_form(psa):
+    lib = psa.cdll()
+    for n in (0, 1, 2047, 2048, 2049, 1 << 24, 86_564_352):
+        nb = -(-n // 2048)
+        assert lib.psadam_state_bytes(0, n) == 8 * n
+        assert lib.psadam_state_bytes(1, n) == 4 * n
+        assert lib.psadam_state_bytes(2, n) == 2 * n + 8 * nb
+    assert lib.psadam_state_bytes(3, 10) == 0 and lib.psadam_state_bytes(0, -1) == 0
+    n = 1 << 24
+    assert 3.99 < lib.psadam_state_bytes(0, n) / lib.psadam_state_bytes(2, n) < 4.0
+
+
+def test_status_strings(psa):
+    assert psa.status_string(0) == "PSADAM_OK"
+    assert psa.status_string(3) == "PSADAM_ERR_UNSUPPORTED"
+    assert psa.status_string(99) == "PSADAM_ERR_UNKNOWN"
+
+
+# ---------------------------------------------------------------- validation (never launches)
+FAKE = 1 << 20  # aligned, never dereferenced: every call below fails validation first
+
+
+def _arr(ctype, vals):
+    a = (ctype * max(len(vals), 1))()
+    for i, x in enumerate(vals):
+        a[i] = x
+    return a
+
+
+def _call_q8(psa, numel=(4096,), ptr=FAKE, step=1, hp=None, block=2048, pct=100.0, sr=0, grad_dtype=0,
+             n_tensors=None):
+    n = len(numel) if n_tensors is None else n_tensors
+    nums = _arr(ctypes.c_int64, list(numel))
+    ptrs = _arr(ctypes.c_void_p, [ptr] * len(numel))
+    lst = psa._List(n, grad_dtype, nums, ctypes.cast(ptrs, psa._PP), ctypes.cast(ptrs, psa._PP))
+    hp = hp or psa._HParams(1e-3, 0.9, 0.999, 1e-8, 0.0)
+    q = psa._Q8Opts(block, sr, 42, pct)
+    P = ctypes.cast(ptrs, psa._PP)
+    return psa.cdll().adam_step_q8(ctypes.byref(lst), P, P, P, P, step, ctypes.byref(hp), ctypes.byref(q), None)
+
+
+def test_validation_errors(psa):
+    E = psa
+    assert _call_q8(psa, n_tensors=0) == E.OK                       # empty list: no-op
+    assert _call_q8(psa, numel=(0, 0)) == E.OK                      # only empty tensors: no-op
+    assert _call_q8(psa, step=0) == E.ERR_INVALID_ARG
+    assert _call_q8(psa, numel=(-1,)) == E.ERR_INVALID_ARG
+    assert _call_q8(psa, ptr=FAKE + 4) == E.ERR_MISALIGNED
+    assert _call_q8(psa, ptr=0) == E.ERR_INVALID_ARG
+    assert _call_q8(psa, block=1024) == E.ERR_UNSUPPORTED
+    assert _call_q8(psa, pct=0.0) == E.ERR_INVALID_ARG
+    assert _call_q8(psa, pct=100.5) == E.ERR_INVALID_ARG
+    assert _call_q8(psa, pct=float("nan")) == E.ERR_INVALID_ARG
+    assert _call_q8(psa, pct=90.0) == E.ERR_UNSUPPORTED             # rank 205 of a full block
+    assert _call_q8(psa, sr=2) == E.ERR_INVALID_ARG
+    assert _call_q8(psa, grad_dtype=5) == E.ERR_INVALID_ARG
+    for bad in ((1e-3, 1.0, 0.999, 1e-8, 0.0), (1e-3, 0.9, -0.1, 1e-8, 0.0), (float("inf"), 0.9, 0.999, 1e-8, 0.0),
+                (1e-3, 0.9, 0.999, -1.0, 0.0)):
+        assert _call_q8(psa, hp=psa._HParams(*bad)) == E.ERR_INVALID_ARG
+    assert psa.cdll().adam_step_q8(None, None, None, None, None, 1, None, None, None) == E.ERR_INVALID_ARG
+    # numel beyond what one grid can cover
+    assert _call_q8(psa, numel=((2 ** 31) * 2048,)) == E.ERR_UNSUPPORTED
+
+
+def test_percentile_rank_limit_follows_the_block(psa):
+    # 99.0 -> rank 21 of a full block: beyond the selectable 16, rejected before launch
+    assert _call_q8(psa, numel=(2048,), pct=99.0) == psa.ERR_UNSUPPORTED
+    assert _call_q8(psa, numel=(5, 2048), pct=99.2) == psa.ERR_UNSUPPORTED  # rank 17

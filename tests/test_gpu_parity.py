@@ -1,0 +1,372 @@
+"""GPU parity: libpsadam.so (called through its C ABI via the thin binding) against the
+CPU oracle on identical seeded inputs, element by element.
+
+Covers every moment mode (fp32, bf16, 8-bit), both grad dtypes, round-to-nearest and
+stochastic rounding, absmax and percentile scaling, ragged multi-tensor lists (sizes
+1, 2, 7, 2047, 2048, 2049, 4097, ...), lists longer than one launch, the quantize-only
+and dequantize-only entry points (bit-exact), exhaustive bf16 rounding through the step
+kernel, resume-equals-uninterrupted, and the workloads at full size (sampled blocks where
+the oracle cannot run the whole tensor; the update is block-local, so a sampled block is
+checked exactly).
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import HParams, Q8Opts
+import workloads
+from parity_util import (assert_codes, assert_moment, assert_params, bf16_bits, compare_state,
+                         device_state_to_host, exact_fraction, host_state, hp_kwargs, q8_kwargs)
+
+pytestmark = pytest.mark.gpu
+
+RAGGED = [1, 2, 7, 2047, 2048, 2049, 4097, 70001]
+
+
+@pytest.fixture(scope="module")
+def psa():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import precision_state_adam_gb300 as psa
+    return psa
+
+
+@pytest.fixture(autouse=True)
+def _free_memory():
+    yield
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+
+
+DEV = "cuda:0"
+
+
+def _to_dev(arrs, dtype=None):
+    out = []
+    for a in arrs:
+        if a.dtype == np.uint16:  # bf16 bits
+            out.append(torch.from_numpy(a.view(np.int16).copy()).to(DEV).view(torch.bfloat16))
+        else:
+            out.append(torch.from_numpy(a.copy()).to(DEV))
+    return out
+
+
+def run_both(psa, mode, sizes, steps, hp, q8=Q8Opts(), grad_dtype="f32", grad_kind="normal", grad_std=1e-2,
+             seed=5, init_state=None):
+    """Run `steps` steps on the GPU and in the oracle from the same inputs; return both."""
+    specs = [workloads.TensorSpec(f"t{i}", (n,)) for i, n in enumerate(sizes)]
+    p_host = workloads.init_params_np(specs, seed=seed)
+    params = _to_dev(p_host)
+    ostate = host_state(mode, sizes) if init_state is None else init_state
+    state = psa.zeros_state(params, mode)
+    if init_state is not None:
+        for k, arrs in enumerate(zip(*init_state)):
+            for i, a in enumerate(arrs):
+                state[k][i].copy_(_to_dev([a])[0])
+    for t in range(1, steps + 1):
+        g32 = workloads.grads_np(sizes, t, grad_std, seed=seed, kind=grad_kind)
+        g_host = [workloads.to_bf16_bits_truncate(g) for g in g32] if grad_dtype == "bf16" else g32
+        grads = _to_dev(g_host)
+        kw = hp_kwargs(hp)
+        if mode == "q8":
+            kw.update(q8_kwargs(q8))
+        psa.adam_step(mode, params, grads, state, t, **kw)
+        oracle.step_list(mode, p_host, g_host, ostate, t, hp, q8)
+    torch.cuda.synchronize()
+    got_p = [p.cpu().numpy() for p in params]
+    got_s = [device_state_to_host(mode, state, i) for i in range(len(sizes))]
+    return got_p, p_host, got_s, ostate
+
+
+def check_all(mode, got_p, want_p, got_s, want_s, what):
+    exact = []
+    for i in range(len(got_p)):
+        assert_params(got_p[i], want_p[i], f"{what} tensor {i}")
+        compare_state(mode, got_s[i], want_s[i], f"{what} tensor {i}")
+        exact.append(exact_fraction(mode, [got_p[i], *got_s[i]], [want_p[i], *want_s[i]]))
+    return min(exact)
+
+
+# ------------------------------------------------------------------ every mode on ragged lists
+@pytest.mark.parametrize("grad_dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("mode", ["fp32", "bf16m"])
+def test_step_ragged_list(psa, mode, grad_dtype):
+    hp = HParams(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01)
+    got_p, want_p, got_s, want_s = run_both(psa, mode, RAGGED, 5, hp, grad_dtype=grad_dtype)
+    ex = check_all(mode, got_p, want_p, got_s, want_s, f"{mode}/{grad_dtype}")
+    assert ex == 1.0, f"expected bit-identical results, exact fraction {ex}"
+
+
+Q8_CASES = {
+    "rne_absmax": Q8Opts(False, 42, 100.0),
+    "sr_absmax": Q8Opts(True, 42, 100.0),
+    "rne_p99.9": Q8Opts(False, 42, 99.9),   # rank 3 of a full block (K = 4 kernel)
+    "sr_p99.9": Q8Opts(True, 7, 99.9),
+    "rne_p99.5": Q8Opts(False, 42, 99.5),   # rank 11 (K = 16 kernel)
+}
+
+
+@pytest.mark.parametrize("grad_dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("case", sorted(Q8_CASES))
+def test_q8_step_ragged_list(psa, case, grad_dtype):
+    hp = HParams(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.1)
+    got_p, want_p, got_s, want_s = run_both(psa, "q8", RAGGED, 5, hp, Q8_CASES[case], grad_dtype=grad_dtype,
+                                            grad_kind="student_t_outliers", grad_std=1e-3)
+    ex = check_all("q8", got_p, want_p, got_s, want_s, f"q8/{case}/{grad_dtype}")
+    assert ex == 1.0, f"expected bit-identical results, exact fraction {ex}"
+
+
+def test_zero_grads_are_pure_decay(psa):
+    n = 10000
+    p0 = workloads.init_params_np([workloads.TensorSpec("w", (n,))], seed=8)[0]
+    for mode in ("fp32", "bf16m", "q8"):
+        params = _to_dev([p0])
+        state = psa.zeros_state(params, mode)
+        want = p0.copy()
+        decay = oracle.scalars(HParams(lr=1e-3, weight_decay=0.1), 1)["decay"]
+        for t in range(1, 4):
+            psa.adam_step(mode, params, [torch.zeros(n, device=DEV)], state, t, lr=1e-3, weight_decay=0.1)
+            want = (want * decay).astype(np.float32)
+        np.testing.assert_array_equal(params[0].cpu().numpy(), want)
+
+
+# ------------------------------------------------------------------ long lists: several launches
+def test_long_list_spans_several_launches(psa):
+    rng = np.random.default_rng(3)
+    sizes = [int(x) for x in rng.integers(1, 3000, size=1000)]
+    sizes[10] = 0  # an empty tensor in the middle of the list
+    hp = HParams(weight_decay=0.01)
+    q8 = Q8Opts(True, 99, 99.9)
+    got_p, want_p, got_s, want_s = run_both(psa, "q8", sizes, 2, hp, q8, grad_std=1e-3)
+    ex = check_all("q8", got_p, want_p, got_s, want_s, "q8 long list")
+    assert ex == 1.0
+
+
+# ------------------------------------------------------------------ quantize / dequantize only
+@pytest.mark.parametrize("case", sorted(Q8_CASES))
+def test_quantize_only_is_bit_exact(psa, case):
+    q8 = Q8_CASES[case]
+    sizes = RAGGED + [2048 * 5]
+    ms, vs = [], []
+    for i, n in enumerate(sizes):
+        m, v = workloads.random_moments_np(n, seed=20 + i)
+        if n == 2048 * 5:
+            m[2048:4096] = 0.0  # an all-zero block
+            v[2048:4096] = 0.0
+            m[:2048] = 3e-4     # a constant block
+            v[4096] = 1.0       # a single outlier
+        ms.append(m)
+        vs.append(v)
+    dm, dv = _to_dev(ms), _to_dev(vs)
+    mc, vc, msc, vsc = psa.zeros_state(dm, "q8")
+    psa.q8_quantize(dm, dv, mc, vc, msc, vsc, step=9, **q8_kwargs(q8))
+    torch.cuda.synchronize()
+    for i, n in enumerate(sizes):
+        want = oracle.quantize(ms[i], vs[i], q8, step=9, tensor_idx=i)
+        got = (mc[i].cpu().numpy(), vc[i].cpu().numpy(), msc[i].cpu().numpy(), vsc[i].cpu().numpy())
+        for g, w, name in zip(got, want, ("m codes", "v codes", "m scales", "v scales")):
+            np.testing.assert_array_equal(np.ascontiguousarray(g).view(np.uint8), np.ascontiguousarray(w).view(np.uint8),
+                                          err_msg=f"{case} tensor {i} {name}")
+
+
+def test_dequantize_only_is_bit_exact(psa):
+    rng = np.random.default_rng(4)
+    sizes = RAGGED
+    mc = [rng.integers(-127, 128, n).astype(np.int8) for n in sizes]
+    vc = [rng.integers(0, 256, n).astype(np.uint8) for n in sizes]
+    msc = [(rng.random(oracle.n_blocks(n)) * 1e-4).astype(np.float32) for n in sizes]
+    vsc = [(rng.random(oracle.n_blocks(n)) * 1e-8).astype(np.float32) for n in sizes]
+    dmc, dvc, dms, dvs = _to_dev(mc), _to_dev(vc), _to_dev(msc), _to_dev(vsc)
+    m = [torch.empty(n, device=DEV) for n in sizes]
+    v = [torch.empty(n, device=DEV) for n in sizes]
+    psa.q8_dequantize(dmc, dvc, dms, dvs, m, v)
+    torch.cuda.synchronize()
+    for i in range(len(sizes)):
+        wm, wv = oracle.dequantize(mc[i], vc[i], msc[i], vsc[i])
+        np.testing.assert_array_equal(m[i].cpu().numpy().view(np.uint32), wm.view(np.uint32))
+        np.testing.assert_array_equal(v[i].cpu().numpy().view(np.uint32), wv.view(np.uint32))
+
+
+# ------------------------------------------------------------------ bf16 rounding, exhaustively
+def test_bf16_store_rounding_exhaustive(psa):
+    """With beta1 = 0 the new m is exactly g (0*m + 1*g), so the stored bf16 m is the
+    kernel's rounding of g. Sweep g over all 2^32 fp32 bit patterns (NaNs only need to
+    stay NaN: GPU arithmetic returns a canonical NaN) against the oracle's rounding."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    chunk = 1 << 28
+    base = np.arange(chunk, dtype=np.uint32)
+    p = torch.zeros(chunk, device=DEV)
+    m = torch.zeros(chunk, dtype=torch.bfloat16, device=DEV)
+    v = torch.zeros(chunk, dtype=torch.bfloat16, device=DEV)
+    dbase = torch.arange(chunk, dtype=torch.int64, device=DEV)
+    pool = ThreadPoolExecutor(max_workers=8)
+    for start in range(0, 1 << 32, chunk):
+        g = dbase + start
+        g = torch.where(g >= 2 ** 31, g - 2 ** 32, g).to(torch.int32).view(torch.float32)
+        m.zero_()  # 0 * (previous chunk's inf/NaN) would not be 0
+        v.zero_()
+        psa.adam_step_bf16m([p], [g], [m], [v], 1, lr=1e-3, beta1=0.0, beta2=0.0, eps=1e-8)
+        got = bf16_bits(m)
+        # m' = 0*0 + 1*g: g itself, except that -0 becomes +0
+        x = (base + np.uint32(start)).view(np.float32) + np.float32(0.0)
+        parts = np.array_split(np.arange(chunk), 8)
+        want = np.concatenate(list(pool.map(lambda ix: oracle.bf16_round(x[ix[0]:ix[-1] + 1]), parts)))
+        nan = np.isnan(x)
+        np.testing.assert_array_equal(got[~nan], want[~nan], err_msg=f"chunk at {start:#x}")
+        assert np.all((got[nan] & 0x7F80) == 0x7F80) and np.all((got[nan] & 0x7F) != 0)
+    pool.shutdown()
+
+
+# ------------------------------------------------------------------ resume
+def test_resume_equals_uninterrupted(psa):
+    """k steps, state copied to the host and back, then N-k steps == N straight steps,
+    bit for bit (stochastic rounding is keyed by (seed, step, index) only)."""
+    sizes = [5000, 2048 * 3]
+    hp = HParams(weight_decay=0.01)
+    q8 = Q8Opts(True, 42, 99.9)
+    specs = [workloads.TensorSpec(f"t{i}", (n,)) for i, n in enumerate(sizes)]
+    p0 = workloads.init_params_np(specs, seed=2)
+    runs = []
+    for split in (None, 3):
+        params = _to_dev(p0)
+        state = psa.zeros_state(params, "q8")
+        for t in range(1, 7):
+            if split is not None and t == split + 1:
+                saved = [[s.cpu() for s in part] for part in state]
+                saved_p = [p.cpu() for p in params]
+                state = [[s.to(DEV) for s in part] for part in saved]
+                params = [p.to(DEV) for p in saved_p]
+            grads = _to_dev(workloads.grads_np(sizes, t, 1e-3, seed=2))
+            psa.adam_step_q8(params, grads, *state, t, **hp_kwargs(hp), **q8_kwargs(q8))
+        runs.append(([p.cpu().numpy() for p in params], [[s.cpu().numpy() for s in part] for part in state]))
+    for a, b in zip(runs[0][0], runs[1][0]):
+        np.testing.assert_array_equal(a, b)
+    for pa, pb in zip(runs[0][1], runs[1][1]):
+        for a, b in zip(pa, pb):
+            np.testing.assert_array_equal(a, b)
+
+
+def test_runs_on_the_callers_stream(psa):
+    n = 300000
+    p0 = workloads.init_params_np([workloads.TensorSpec("w", (n,))], seed=6)[0]
+    g = workloads.grads_np([n], 1, 1e-2, seed=6)[0]
+    outs = []
+    for use_side in (False, True):
+        params = _to_dev([p0])
+        grads = _to_dev([g])
+        state = psa.zeros_state(params, "bf16m")
+        s = torch.cuda.Stream() if use_side else torch.cuda.current_stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            psa.adam_step_bf16m(params, grads, *state, 1)
+        s.synchronize()
+        outs.append(params[0].cpu().numpy())
+    np.testing.assert_array_equal(outs[0], outs[1])
+
+
+# ------------------------------------------------------------------ the workloads at full size
+def test_flat_1m_bf16m_full(psa):
+    w = workloads.WORKLOADS["flat_1m"]
+    hp = HParams(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay)
+    got_p, want_p, got_s, want_s = run_both(psa, "bf16m", w.sizes, w.steps, hp, grad_std=w.grad_std, seed=1234)
+    check_all("bf16m", got_p, want_p, got_s, want_s, "flat_1m")
+
+
+def test_flat_16m_q8_full(psa):
+    w = workloads.WORKLOADS["flat_16m"]
+    hp = HParams(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay)
+    got_p, want_p, got_s, want_s = run_both(psa, "q8", w.sizes, w.steps, hp, Q8Opts(False, 42, 100.0),
+                                            grad_std=w.grad_std, seed=1234)
+    check_all("q8", got_p, want_p, got_s, want_s, "flat_16m")
+
+
+def _sample_blocks(nb: int):
+    return sorted({0, nb - 1, *range(0, nb, 257)})
+
+
+def sampled_run(psa, w: workloads.Workload, mode: str, steps: int, tensor_stride: int = 1):
+    """Full-size GPU run of workload `w` in moment mode `mode`, with the oracle following a
+    deterministic sample of blocks (block 0, the last, every 257th) of every
+    `tensor_stride`-th tensor. Inputs come from the device generators of the benchmark."""
+    dev = torch.device(DEV)
+    sizes = w.sizes
+    params = workloads.init_params_torch(w.specs, dev)
+    state = psa.zeros_state(params, mode)
+    hp = HParams(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay)
+    q8 = Q8Opts(w.stochastic_rounding, w.seed, w.percentile)
+    picks = []  # (tensor index, block index, start, length)
+    for i in range(0, len(sizes), tensor_stride):
+        nb = oracle.n_blocks(sizes[i])
+        for b in _sample_blocks(nb):
+            lo = b * 2048
+            picks.append((i, b, lo, min(2048, sizes[i] - lo)))
+    host = {}
+    for (i, b, lo, ln) in picks:
+        p = params[i][lo:lo + ln].cpu().numpy().copy()
+        if mode == "fp32":
+            st = [np.zeros(ln, np.float32), np.zeros(ln, np.float32)]
+        elif mode == "bf16m":
+            st = [np.zeros(ln, np.uint16), np.zeros(ln, np.uint16)]
+        else:
+            st = [np.zeros(ln, np.int8), np.zeros(ln, np.uint8), np.zeros(1, np.float32), np.zeros(1, np.float32)]
+        host[(i, b)] = (p, st)
+    gbuf = [torch.empty(n, dtype=torch.float32 if w.grad_dtype == "f32" else torch.bfloat16, device=dev)
+            for n in sizes]
+    for t in range(1, steps + 1):
+        workloads.grads_torch(sizes, t, w.grad_std, dev, kind=w.grad_kind, dtype=w.grad_dtype, out=gbuf)
+        kw = hp_kwargs(hp)
+        if mode == "q8":
+            kw.update(q8_kwargs(q8))
+        psa.adam_step(mode, params, gbuf, state, t, **kw)
+        for (i, b, lo, ln) in picks:
+            gs = gbuf[i][lo:lo + ln]
+            g = bf16_bits(gs) if w.grad_dtype == "bf16" else gs.cpu().numpy()
+            p, st = host[(i, b)]
+            if mode == "fp32":
+                oracle.step_fp32(p, g, *st, t, hp)
+            elif mode == "bf16m":
+                oracle.step_bf16m(p, g, *st, t, hp)
+            else:
+                oracle.step_q8_block(p, g, *st, t, hp, q8, tensor_idx=i, elem0=lo)
+    torch.cuda.synchronize()
+    exact = 1.0
+    for (i, b, lo, ln) in picks:
+        p, st = host[(i, b)]
+        got_p = params[i][lo:lo + ln].cpu().numpy()
+        if mode == "q8":
+            got_s = (state[0][i][lo:lo + ln].cpu().numpy(), state[1][i][lo:lo + ln].cpu().numpy(),
+                     state[2][i][b:b + 1].cpu().numpy(), state[3][i][b:b + 1].cpu().numpy())
+        elif mode == "bf16m":
+            got_s = (bf16_bits(state[0][i][lo:lo + ln]), bf16_bits(state[1][i][lo:lo + ln]))
+        else:
+            got_s = (state[0][i][lo:lo + ln].cpu().numpy(), state[1][i][lo:lo + ln].cpu().numpy())
+        what = f"{w.name}/{mode} tensor {i} block {b}"
+        assert_params(got_p, p, what)
+        compare_state(mode, got_s, tuple(st), what)
+        exact = min(exact, exact_fraction(mode, [got_p, *got_s], [p, *st]))
+    del params, state, gbuf
+    return exact, len(picks)
+
+
+def test_vit_base_list_sampled(psa):
+    w = workloads.WORKLOADS["vit_base"]
+    for mode in ("bf16m", "fp32", "q8"):
+        exact, n = sampled_run(psa, w, mode, steps=w.steps if mode == "bf16m" else 10, tensor_stride=3)
+        assert exact == 1.0 and n > 100
+
+
+def test_flat_1g_heavy_tail_sr_sampled(psa):
+    w = workloads.WORKLOADS["flat_1g_heavy"]
+    exact, n = sampled_run(psa, w, "q8", steps=w.steps)
+    assert exact == 1.0 and n > 2000
+
+
+@pytest.mark.parametrize("mode", ["fp32", "bf16m", "q8"])
+def test_gpt_1p3b_bf16_grads_sampled(psa, mode):
+    w = workloads.WORKLOADS["gpt_1p3b"]
+    exact, n = sampled_run(psa, w, mode, steps=w.steps, tensor_stride=5)
+    assert exact == 1.0 and n > 200
