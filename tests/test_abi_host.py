@@ -14,8 +14,8 @@ HEADER = os.path.join(ROOT, "include", "psadam.h")
 
 @pytest.fixture(scope="module")
 def psa():
-    from precision_state_adam_gb300 import build
-    build.build()
+    import __graft_entry__
+    __graft_entry__.build()
     import precision_state_adam_gb300 as psa
     return psa
 
