@@ -212,7 +212,8 @@ def test_bf16_store_rounding_exhaustive(psa):
         psa.adam_step_bf16m([p], [g], [m], [v], 1, lr=1e-3, beta1=0.0, beta2=0.0, eps=1e-8)
         got = bf16_bits(m)
         # m' = 0*0 + 1*g: g itself, except that -0 becomes +0
-        x = (base + np.uint32(start)).view(np.float32) + np.float32(0.0)
+        with np.errstate(invalid="ignore"):
+            x = (base + np.uint32(start)).view(np.float32) + np.float32(0.0)
         parts = np.array_split(np.arange(chunk), 8)
         want = np.concatenate(list(pool.map(lambda ix: oracle.bf16_round(x[ix[0]:ix[-1] + 1]), parts)))
         nan = np.isnan(x)
@@ -355,8 +356,8 @@ def sampled_run(psa, w: workloads.Workload, mode: str, steps: int, tensor_stride
 def test_vit_base_list_sampled(psa):
     w = workloads.WORKLOADS["vit_base"]
     for mode in ("bf16m", "fp32", "q8"):
-        exact, n = sampled_run(psa, w, mode, steps=w.steps if mode == "bf16m" else 10, tensor_stride=3)
-        assert exact == 1.0 and n > 100
+        exact, n = sampled_run(psa, w, mode, steps=w.steps if mode == "bf16m" else 10, tensor_stride=2)
+        assert exact == 1.0 and n > 90
 
 
 def test_flat_1g_heavy_tail_sr_sampled(psa):
