@@ -135,6 +135,23 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
+# ------------------------------------------------------------------ multi-rank aggregation
+def max_over_ranks(seconds: float, dist, device) -> float:
+    """The slowest rank's time: every rank passes its own, all get the max."""
+    if dist is None:
+        return seconds
+    import torch
+    t = torch.tensor([seconds], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gparams_per_s(params_per_rank: int, steps: int, seconds: float, world: int) -> float:
+    """Whole-job throughput: every rank updates its own shard of `params_per_rank`
+    params per step (weak scaling), timed by the slowest rank."""
+    return world * params_per_rank * steps / seconds / 1e9
+
+
 # ------------------------------------------------------------------ our implementation
 def run_ours(args, rank: int, world: int, dist):
     import torch
@@ -190,15 +207,11 @@ def run_ours(args, rank: int, world: int, dist):
         if dist is not None:
             dist.barrier()
         step_ms = [a.elapsed_time(b) for a, b in evs]
-        total_s = sum(step_ms) / 1e3
-        if dist is not None:
-            tt = torch.tensor([total_s], dtype=torch.float64, device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            total_s = float(tt.item())
+        total_s = max_over_ranks(sum(step_ms) / 1e3, dist, dev)
         nbytes = algorithmic_bytes(mode, sizes, w.grad_dtype)
         mean_s = sum(step_ms) / len(step_ms) / 1e3
         results[mode] = {
-            "gparams_per_s": world * numel * args.steps / total_s / 1e9,
+            "gparams_per_s": job_gparams_per_s(numel, args.steps, total_s, world),
             "ms_per_step": total_s * 1e3 / args.steps,
             "median_ms": statistics.median(step_ms),
             "bytes_per_step": nbytes,
@@ -249,12 +262,8 @@ def run_e2e(args, psa, torch, dev, stream, w, params, state, kw, t, flush, dist,
         e1.record(stream)
         e1.synchronize()
         ms.append(e0.elapsed_time(e1))
-    total_s = sum(ms) / 1e3
-    if dist is not None:
-        tt = torch.tensor([total_s], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_s = float(tt.item())
-    return {"value": round(world * sum(sizes) * args.steps / total_s / 1e9, 3), "unit": "Gparams/s",
+    total_s = max_over_ranks(sum(ms) / 1e3, dist, dev)
+    return {"value": round(job_gparams_per_s(sum(sizes), args.steps, total_s, world), 3), "unit": "Gparams/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
 
