@@ -185,10 +185,12 @@ def run_ours(args, rank: int, world: int, dist):
         if mode == "q8":
             kw.update(stochastic_rounding=w.stochastic_rounding, seed=w.seed, percentile=w.percentile)
         launches_per_step = -(-len([n for n in sizes if n > 0]) // (8 if len(sizes) <= 8 else 440))
+        # one marshalled plan per grad set: a step is then a single C call
+        plans = [psa.StepPlan(mode, params, grads[s], state, **kw) for s in range(n_sets)]
         t = 0
         for _ in range(args.warmup):
             t += 1
-            psa.adam_step(mode, params, grads[(t - 1) % n_sets], state, t, **kw)
+            plans[(t - 1) % n_sets].step(t)
         torch.cuda.synchronize(dev)
         if dist is not None:
             dist.barrier()
@@ -200,7 +202,7 @@ def run_ours(args, rank: int, world: int, dist):
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
             e0.record(stream)
-            psa.adam_step(mode, params, grads[(t - 1) % n_sets], state, t, **kw)
+            plans[(t - 1) % n_sets].step(t)
             e1.record(stream)
             evs.append((e0, e1))
         torch.cuda.synchronize(dev)
@@ -221,6 +223,7 @@ def run_ours(args, rank: int, world: int, dist):
         # ---- end to end through the public API with host buffers
         if mode == args.modes[0]:
             results[mode]["e2e"] = run_e2e(args, psa, torch, dev, stream, w, params, state, kw, t, flush, dist, world)
+        del plans
             results[mode]["launches"] += launches_per_step * args.steps
         del params, state
         torch.cuda.empty_cache()
@@ -235,13 +238,14 @@ def run_e2e(args, psa, torch, dev, stream, w, params, state, kw, t, flush, dist,
     host_g = [[g.cpu().pin_memory() for g in gs] for gs in host_g]
     host_p = [torch.empty(p.numel(), dtype=torch.float32, pin_memory=True) for p in params]
     dev_g = [torch.empty(n, dtype=gdt, device=dev) for n in sizes]
+    plan = psa.StepPlan(args.modes[0], params, dev_g, state, **kw)
     h2d = sum(g.numel() * g.element_size() for g in host_g[0])
     d2h = sum(p.numel() * 4 for p in params)
     for i in range(3):  # warm the copy engines
         t += 1
         for d, h in zip(dev_g, host_g[i % 2]):
             d.copy_(h, non_blocking=True)
-        psa.adam_step(args.modes[0], params, dev_g, state, t, **kw)
+        plan.step(t)
         for h, p in zip(host_p, params):
             h.copy_(p, non_blocking=True)
     torch.cuda.synchronize(dev)
@@ -256,7 +260,7 @@ def run_e2e(args, psa, torch, dev, stream, w, params, state, kw, t, flush, dist,
         e0.record(stream)
         for d, h in zip(dev_g, host_g[i % 2]):
             d.copy_(h, non_blocking=True)
-        psa.adam_step(args.modes[0], params, dev_g, state, t, **kw)
+        plan.step(t)
         for h, p in zip(host_p, params):
             h.copy_(p, non_blocking=True)
         e1.record(stream)
@@ -336,11 +340,22 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="flat_16m", choices=sorted(workloads.WORKLOADS))
     ap.add_argument("--modes", default=None, help="comma list; the first is the headline (default: workload's)")
+    ap.add_argument("--numel", type=int, default=None,
+                    help="resize a one-tensor workload (for profiling small cases)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-step-seconds", type=float, default=3.0)
     args = ap.parse_args()
     w = workloads.WORKLOADS[args.workload]
+    if args.numel is not None:
+        if len(w.specs) != 1:
+            raise SystemExit("--numel applies to one-tensor workloads only")
+        import dataclasses
+        w = dataclasses.replace(w, name=f"{w.name}@{args.numel}",
+                                specs=(workloads.TensorSpec(w.specs[0].name, (args.numel,)),),
+                                description=w.description + f" (resized to {args.numel:,} params)")
+        workloads.WORKLOADS[w.name] = w
+        args.workload = w.name
     if args.modes is None:
         rest = [m for m in ("q8", "bf16m", "fp32") if m != w.mode]
         args.modes = [w.mode] + rest

@@ -264,6 +264,62 @@ def adam_step(mode: str, params, grads, state, step: int, **kw) -> None:
         raise ValueError(f"unknown moment mode {mode!r}")
 
 
+class StepPlan:
+    """A tensor list marshalled once for repeated steps.
+
+    Building the pointer tables costs Python time proportional to the number of tensors;
+    an optimizer calls the step with the same tensors every iteration, so the plan keeps
+    the tables and each :meth:`step` is one C call. The tensors must stay alive and in
+    place (same storage) for the plan's lifetime; grads may be swapped with
+    :meth:`set_grads` (same shapes and dtype)."""
+
+    def __init__(self, mode: str, params, grads, state, lr: float = 1e-3, beta1: float = 0.9,
+                 beta2: float = 0.999, eps: float = 1e-8, weight_decay: float = 0.0,
+                 stochastic_rounding: bool = False, seed: int = 42, percentile: float = 100.0,
+                 block_size: int = BLOCK):
+        if mode not in MODES:
+            raise ValueError(f"unknown moment mode {mode!r}")
+        self.mode = mode
+        self._lst, self._keep = _list(params, grads)
+        self._grad_dtype = grads[0].dtype if grads else torch.float32
+        self._params = list(params)
+        if mode == "fp32":
+            _check_layout("m", state[0], torch.float32, params)
+            _check_layout("v", state[1], torch.float32, params)
+        elif mode == "bf16m":
+            _check_layout("m", state[0], torch.bfloat16, params)
+            _check_layout("v", state[1], torch.bfloat16, params)
+        else:
+            _check_layout("m_code", state[0], torch.int8, params)
+            _check_layout("v_code", state[1], torch.uint8, params)
+            _check_layout("m_scale", state[2], torch.float32, params, n_blocks)
+            _check_layout("v_scale", state[3], torch.float32, params, n_blocks)
+        self._state_ptrs = [_ptrs(x) for x in state]
+        self._state_pp = [ctypes.cast(p, _PP) for p in self._state_ptrs]
+        self._state = state
+        self._hp = _hp(lr, beta1, beta2, eps, weight_decay)
+        self._q8 = _q8(stochastic_rounding, seed, percentile, block_size)
+
+    def set_grads(self, grads) -> None:
+        if len(grads) != len(self._params):
+            raise ValueError("grads differ in length from params")
+        _check_layout("grads", grads, self._grad_dtype, self._params)
+        gp = _ptrs(grads)
+        self._keep = (self._keep[0], self._keep[1], gp)
+        self._lst.grad = ctypes.cast(gp, _PP)
+
+    def step(self, step: int, stream=None) -> None:
+        h = _stream_handle(stream, self._params)
+        if self.mode == "fp32":
+            st = _lib.adam_step_fp32(ctypes.byref(self._lst), *self._state_pp, step, ctypes.byref(self._hp), h)
+        elif self.mode == "bf16m":
+            st = _lib.adam_step_bf16m(ctypes.byref(self._lst), *self._state_pp, step, ctypes.byref(self._hp), h)
+        else:
+            st = _lib.adam_step_q8(ctypes.byref(self._lst), *self._state_pp, step, ctypes.byref(self._hp),
+                                   ctypes.byref(self._q8), h)
+        _raise(st, f"StepPlan.step ({self.mode})")
+
+
 def cdll() -> ctypes.CDLL:
     """The loaded libpsadam.so handle (for ABI-level tests)."""
     return _lib
