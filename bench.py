@@ -223,9 +223,8 @@ def run_ours(args, rank: int, world: int, dist):
         # ---- end to end through the public API with host buffers
         if mode == args.modes[0]:
             results[mode]["e2e"] = run_e2e(args, psa, torch, dev, stream, w, params, state, kw, t, flush, dist, world)
-        del plans
             results[mode]["launches"] += launches_per_step * args.steps
-        del params, state
+        del plans, params, state
         torch.cuda.empty_cache()
     clk = clocks.stop()
     return results, clk
