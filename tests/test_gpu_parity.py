@@ -371,3 +371,32 @@ def test_gpt_1p3b_bf16_grads_sampled(psa, mode):
     w = workloads.WORKLOADS["gpt_1p3b"]
     exact, n = sampled_run(psa, w, mode, steps=w.steps, tensor_stride=5)
     assert exact == 1.0 and n > 200
+
+
+def test_step_plan_matches_direct_calls(psa):
+    """The cached StepPlan issues the same C call as the one-shot binding: identical results."""
+    sizes = [3000, 1, 2048 * 2 + 5]
+    specs = [workloads.TensorSpec(f"t{i}", (n,)) for i, n in enumerate(sizes)]
+    p0 = workloads.init_params_np(specs, seed=17)
+    q8 = Q8Opts(True, 3, 99.9)
+    for mode in ("fp32", "bf16m", "q8"):
+        runs = []
+        for use_plan in (False, True):
+            params = _to_dev(p0)
+            state = psa.zeros_state(params, mode)
+            gbufs = [_to_dev(workloads.grads_np(sizes, t, 1e-2, seed=17)) for t in (1, 2, 3)]
+            kw = dict(weight_decay=0.01)
+            if mode == "q8":
+                kw.update(q8_kwargs(q8))
+            if use_plan:
+                plan = psa.StepPlan(mode, params, gbufs[0], state, **kw)
+                for t in (1, 2, 3):
+                    plan.set_grads(gbufs[t - 1])
+                    plan.step(t)
+            else:
+                for t in (1, 2, 3):
+                    psa.adam_step(mode, params, gbufs[t - 1], state, t, **kw)
+            torch.cuda.synchronize()
+            runs.append([p.cpu().numpy() for p in params])
+        for a, b in zip(*runs):
+            np.testing.assert_array_equal(a, b)
