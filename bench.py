@@ -40,17 +40,18 @@ import workloads  # noqa: E402
 
 METRIC = "Gparams/s per AdamW step and achieved HBM GB/s (% of GB300 peak), per moment mode"
 L2_FLUSH_BYTES = 384 << 20
-STATE_BYTES = {"fp32": 4, "bf16m": 2, "q8": 1}   # per moment element
+STATE_BYTES = {"fp32": (4, 4), "bf16m": (2, 2), "q8": (1, 1), "q8v": (4, 1)}   # per m, v element
 
 
 def algorithmic_bytes(mode: str, sizes, grad_dtype: str) -> int:
     """Bytes the step must move once each: p read+write, g read, m and v read+write,
     and for 8-bit moments the two fp32 scales of every block read+write."""
     g = 4 if grad_dtype == "f32" else 2
-    per = 8 + g + 4 * STATE_BYTES[mode]
+    mb, vb = STATE_BYTES[mode]
+    per = 8 + g + 2 * mb + 2 * vb
     total = per * sum(sizes)
-    if mode == "q8":
-        total += 16 * sum((n + 2047) // 2048 for n in sizes)
+    scales = {"q8": 2, "q8v": 1}.get(mode, 0)  # fp32 scale arrays, read + written per block
+    total += 8 * scales * sum((n + 2047) // 2048 for n in sizes)
     return total
 
 
@@ -182,7 +183,7 @@ def run_ours(args, rank: int, world: int, dist):
         params = workloads.init_params_torch(w.specs, dev, seed=workloads.DEFAULT_SEED + rank)
         state = psa.zeros_state(params, mode)
         kw = dict(lr=w.lr, beta1=w.beta1, beta2=w.beta2, eps=w.eps, weight_decay=w.weight_decay)
-        if mode == "q8":
+        if mode in ("q8", "q8v"):
             kw.update(stochastic_rounding=w.stochastic_rounding, seed=w.seed, percentile=w.percentile)
         launches_per_step = -(-len([n for n in sizes if n > 0]) // (8 if len(sizes) <= 8 else 440))
         # one marshalled plan per grad set: a step is then a single C call
@@ -284,6 +285,8 @@ def oracle_sample_rate(w: workloads.Workload, mode: str, budget_s: float):
         st = [np.zeros(n, np.float32), np.zeros(n, np.float32)]
     elif mode == "bf16m":
         st = [np.zeros(n, np.uint16), np.zeros(n, np.uint16)]
+    elif mode == "q8v":
+        st = [np.zeros(n, np.float32), np.zeros(n, np.uint8), np.zeros(oracle.n_blocks(n), np.float32)]
     else:
         nb = oracle.n_blocks(n)
         st = [np.zeros(n, np.int8), np.zeros(n, np.uint8), np.zeros(nb, np.float32), np.zeros(nb, np.float32)]
@@ -356,7 +359,7 @@ def main():
         workloads.WORKLOADS[w.name] = w
         args.workload = w.name
     if args.modes is None:
-        rest = [m for m in ("q8", "bf16m", "fp32") if m != w.mode]
+        rest = [m for m in ("q8", "bf16m", "fp32", "q8v") if m != w.mode]
         args.modes = [w.mode] + rest
     else:
         args.modes = args.modes.split(",")

@@ -7,6 +7,7 @@
  *   adam_step_fp32   fp32 m and v                                (28 bytes moved / param)
  *   adam_step_bf16m  bf16 m and v, round to nearest even         (20 bytes / param)
  *   adam_step_q8     8-bit block-wise codes + fp32 block scales  (16 bytes / param + scales)
+ *   adam_step_q8v    fp32 m, 8-bit v codes + scales              (22 bytes / param + scales)
  * (byte counts for fp32 grads; bf16 grads move 2 bytes less.)
  *
  * Sources of the method:
@@ -123,6 +124,14 @@ int adam_step_q8(const psadam_list* list, int8_t* const* m_code, uint8_t* const*
                  float* const* m_scale, float* const* v_scale, int64_t step,
                  const psadam_hparams* hp, const psadam_q8_opts* q8, void* stream);
 
+/* One AdamW step keeping the first moment in fp32 and only the second moment 8-bit (PR
+ * #814's "Option to keep first moment in full precision (CompressBothMoments=false)").
+ * m: device float[numel]; v_code: device uint8_t[numel]; v_scale: device
+ * float[ceil(numel/2048)]; all updated in place. v is encoded exactly as adam_step_q8
+ * encodes it (same percentile rule, rounding and stochastic-rounding stream, moment 1). */
+int adam_step_q8v(const psadam_list* list, float* const* m, uint8_t* const* v_code, float* const* v_scale,
+                  int64_t step, const psadam_hparams* hp, const psadam_q8_opts* q8, void* stream);
+
 /* Quantize-only (PR #814's Quantize(m), Quantize(v)): encodes fp32 m, v into codes and
  * scales exactly as adam_step_q8 encodes m', v' (same rounding, percentile and, for
  * stochastic rounding, the same Philox stream for `step`). For state initialisation
@@ -140,7 +149,8 @@ int psadam_q8_dequantize(int32_t n_tensors, const int64_t* numel, const int8_t* 
                          void* stream);
 
 /* Bytes of optimizer state for a tensor of numel params (PR #814's GetMemoryUsage):
- * mode 0 = fp32 (8*numel), 1 = bf16 (4*numel), 2 = 8-bit (2*numel + 8*ceil(numel/2048)).
+ * mode 0 = fp32 (8*numel), 1 = bf16 (4*numel), 2 = 8-bit (2*numel + 8*ceil(numel/2048)),
+ * 3 = fp32 m + 8-bit v (5*numel + 4*ceil(numel/2048)).
  * Returns 0 for an unknown mode or numel < 0. */
 size_t psadam_state_bytes(int32_t mode, int64_t numel);
 

@@ -91,6 +91,8 @@ def _load() -> ctypes.CDLL:
         "orc_step_q8": (None, [i64, _f32p, vp, i32, _i8p, _u8p, _f32p, _f32p, hp, i64, q8, i32,
                                i64, i64]),
         "orc_step_q8_block": (None, [i64, i64, _f32p, vp, i32, _i8p, _u8p, _f32p, _f32p, hp, i64, q8, i32]),
+        "orc_step_q8v": (None, [i64, _f32p, vp, i32, _f32p, _u8p, _f32p, hp, i64, q8, i32, i64, i64]),
+        "orc_step_q8v_block": (None, [i64, i64, _f32p, vp, i32, _f32p, _u8p, _f32p, hp, i64, q8, i32]),
         "orc_probe_mul_add": (ctypes.c_float, [ctypes.c_float] * 3),
     }
     for name, (res, args) in sigs.items():
@@ -269,10 +271,40 @@ def step_q8_block(p, g, mc, vc, ms, vs, t: int, hp: HParams, q8: Q8Opts, tensor_
                            ctypes.byref(hp._c()), t, ctypes.byref(q8._c()), tensor_idx)
 
 
+def step_q8v(p, g, m, vc, vs, t: int, hp: HParams, q8: Q8Opts = Q8Opts(), tensor_idx: int = 0,
+             blocks: tuple[int, int] | None = None) -> None:
+    """fp32 m, 8-bit v (CompressBothMoments = false) over blocks [b0, b1) of one tensor."""
+    n = p.size
+    _check(p, np.float32, "param")
+    _check(m, np.float32, "m", n)
+    _check(vc, np.uint8, "v_code", n)
+    _check(vs, np.float32, "v_scale", n_blocks(n))
+    b0, b1 = blocks if blocks is not None else (0, n_blocks(n))
+    assert 0 <= b0 <= b1 <= n_blocks(n)
+    gp, gb = _grad(g, n)
+    _lib.orc_step_q8v(n, _ptr(p, ctypes.c_float), gp, gb, _ptr(m, ctypes.c_float), _ptr(vc, ctypes.c_uint8),
+                      _ptr(vs, ctypes.c_float), ctypes.byref(hp._c()), t, ctypes.byref(q8._c()), tensor_idx, b0, b1)
+
+
+def step_q8v_block(p, g, m, vc, vs, t: int, hp: HParams, q8: Q8Opts, tensor_idx: int, elem0: int) -> None:
+    """One block of the fp32-m / 8-bit-v step, held in its own arrays (see step_q8_block)."""
+    n = p.size
+    assert 0 < n <= BLOCK and elem0 % BLOCK == 0
+    _check(p, np.float32, "param")
+    _check(m, np.float32, "m", n)
+    _check(vc, np.uint8, "v_code", n)
+    _check(vs, np.float32, "v_scale", 1)
+    gp, gb = _grad(g, n)
+    _lib.orc_step_q8v_block(n, elem0, _ptr(p, ctypes.c_float), gp, gb, _ptr(m, ctypes.c_float),
+                            _ptr(vc, ctypes.c_uint8), _ptr(vs, ctypes.c_float), ctypes.byref(hp._c()), t,
+                            ctypes.byref(q8._c()), tensor_idx)
+
+
 # ---------------------------------------------------------------- multi-tensor lists
 def step_list(mode: str, params, grads, state, t: int, hp: HParams, q8: Q8Opts = Q8Opts()) -> None:
     """Step a list of tensors; tensor i of the list is tensor_idx i of the stochastic-rounding
-    stream. ``state[i]`` is (m, v) for fp32/bf16m and (mc, vc, ms, vs) for q8."""
+    stream. ``state[i]`` is (m, v) for fp32/bf16m, (mc, vc, ms, vs) for q8 and (m, vc, vs)
+    for q8v (fp32 m, 8-bit v)."""
     for i, (p, g, st) in enumerate(zip(params, grads, state)):
         if mode == "fp32":
             step_fp32(p, g, *st, t, hp)
@@ -280,6 +312,8 @@ def step_list(mode: str, params, grads, state, t: int, hp: HParams, q8: Q8Opts =
             step_bf16m(p, g, *st, t, hp)
         elif mode == "q8":
             step_q8(p, g, *st, t, hp, q8, tensor_idx=i)
+        elif mode == "q8v":
+            step_q8v(p, g, *st, t, hp, q8, tensor_idx=i)
         else:
             raise ValueError(mode)
 

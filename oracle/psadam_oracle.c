@@ -311,4 +311,29 @@ void orc_step_q8(int64_t n, float* p, const void* grad, int grad_bf16, int8_t* m
     }
 }
 
+/* [P814] summary: "Option to keep first moment in full precision
+ * (CompressBothMoments=false)": m stays fp32, only v is block-quantized. Same step order
+ * (dequantize v, update, quantize v), same v encoding and stream as the 8-bit step. */
+void orc_step_q8v_block(int64_t cnt, int64_t elem0, float* p, const void* grad, int grad_bf16, float* m,
+                        uint8_t* v_code, float* v_scale, const orc_hparams* hp, int64_t t,
+                        const orc_q8opts* q, int tensor_idx) {
+    orc_scalars s = orc_make_scalars(hp, t);
+    float vf[ORC_BLOCK];
+    for (int64_t i = 0; i < cnt; ++i) vf[i] = (float)v_code[i] * *v_scale;
+    for (int64_t i = 0; i < cnt; ++i) adam_element(&p[i], load_grad(grad, grad_bf16, i), &m[i], &vf[i], &s);
+    *v_scale = orc_quantize_block(vf, cnt, 0, q, t, tensor_idx, elem0, NULL, v_code);
+}
+
+void orc_step_q8v(int64_t n, float* p, const void* grad, int grad_bf16, float* m, uint8_t* v_code,
+                  float* v_scale, const orc_hparams* hp, int64_t t, const orc_q8opts* q, int tensor_idx,
+                  int64_t block_begin, int64_t block_end) {
+    size_t gsize = grad_bf16 ? sizeof(uint16_t) : sizeof(float);
+    for (int64_t b = block_begin; b < block_end; ++b) {
+        int64_t lo = b * ORC_BLOCK;
+        int64_t cnt = n - lo < ORC_BLOCK ? n - lo : ORC_BLOCK;
+        orc_step_q8v_block(cnt, lo, p + lo, (const char*)grad + (size_t)lo * gsize, grad_bf16, m + lo,
+                           v_code + lo, v_scale + b, hp, t, q, tensor_idx);
+    }
+}
+
 float orc_probe_mul_add(float a, float b, float c) { return a * b + c; }

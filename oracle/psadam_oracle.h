@@ -102,6 +102,15 @@ void orc_step_q8_block(int64_t cnt, int64_t elem0, float* p, const void* grad, i
                        int8_t* m_code, uint8_t* v_code, float* m_scale, float* v_scale,
                        const orc_hparams* hp, int64_t t, const orc_q8opts* q, int tensor_idx);
 
+/* fp32 first moment, 8-bit second moment (the pages' CompressBothMoments = false):
+ * whole-tensor (block range) and single-block forms, arguments as for the 8-bit step. */
+void orc_step_q8v(int64_t n, float* p, const void* grad, int grad_bf16, float* m, uint8_t* v_code,
+                  float* v_scale, const orc_hparams* hp, int64_t t, const orc_q8opts* q, int tensor_idx,
+                  int64_t block_begin, int64_t block_end);
+void orc_step_q8v_block(int64_t cnt, int64_t elem0, float* p, const void* grad, int grad_bf16, float* m,
+                        uint8_t* v_code, float* v_scale, const orc_hparams* hp, int64_t t,
+                        const orc_q8opts* q, int tensor_idx);
+
 /* Build-flag probe: returns a*b + c with two roundings. A build that let the
  * compiler contract this into one fused multiply-add would return the fused value. */
 float orc_probe_mul_add(float a, float b, float c);

@@ -9,6 +9,7 @@ Entry points (same names as the C ABI):
     adam_step_fp32(params, grads, m, v, step, ...)              fp32 moments
     adam_step_bf16m(params, grads, m, v, step, ...)             bf16 moments (torch.bfloat16 tensors)
     adam_step_q8(params, grads, m_code, v_code, m_scale, v_scale, step, ...)
+    adam_step_q8v(params, grads, m, v_code, v_scale, step, ...) fp32 m, 8-bit v
     q8_quantize / q8_dequantize                                 8-bit state conversion
     state_bytes(mode, numel)                                    optimizer-state footprint
 and helpers to allocate fresh (zero) state with the right dtypes and shapes.
@@ -28,7 +29,7 @@ MAX_PERCENTILE_RANK = 16
 
 OK, ERR_INVALID_ARG, ERR_MISALIGNED, ERR_UNSUPPORTED, ERR_CUDA = range(5)
 GRAD_F32, GRAD_BF16 = 0, 1
-MODES = {"fp32": 0, "bf16m": 1, "q8": 2}
+MODES = {"fp32": 0, "bf16m": 1, "q8": 2, "q8v": 3}
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(
@@ -61,6 +62,8 @@ _SIGS = {
     "adam_step_bf16m": [ctypes.POINTER(_List), _PP, _PP, ctypes.c_int64, ctypes.POINTER(_HParams), _vp],
     "adam_step_q8": [ctypes.POINTER(_List), _PP, _PP, _PP, _PP, ctypes.c_int64, ctypes.POINTER(_HParams),
                      ctypes.POINTER(_Q8Opts), _vp],
+    "adam_step_q8v": [ctypes.POINTER(_List), _PP, _PP, _PP, ctypes.c_int64, ctypes.POINTER(_HParams),
+                      ctypes.POINTER(_Q8Opts), _vp],
     "psadam_q8_quantize": [ctypes.c_int32, _I64P, _PP, _PP, _PP, _PP, _PP, _PP, ctypes.POINTER(_Q8Opts),
                            ctypes.c_int64, _vp],
     "psadam_q8_dequantize": [ctypes.c_int32, _I64P, _PP, _PP, _PP, _PP, _PP, _PP, _vp],
@@ -205,6 +208,23 @@ def adam_step_q8(params, grads, m_code, v_code, m_scale, v_scale, step: int, lr:
     _raise(st, "adam_step_q8")
 
 
+def adam_step_q8v(params, grads, m, v_code, v_scale, step: int, lr: float = 1e-3, beta1: float = 0.9,
+                  beta2: float = 0.999, eps: float = 1e-8, weight_decay: float = 0.0, stochastic_rounding: bool = False,
+                  seed: int = 42, percentile: float = 100.0, block_size: int = BLOCK, stream=None) -> None:
+    """One AdamW step with an fp32 first moment and an 8-bit block-wise second moment
+    (uint8 v codes, fp32 per-block scales), in place."""
+    lst, keep = _list(params, grads)
+    _check_layout("m", m, torch.float32, params)
+    _check_layout("v_code", v_code, torch.uint8, params)
+    _check_layout("v_scale", v_scale, torch.float32, params, n_blocks)
+    ptrs = [_ptrs(x) for x in (m, v_code, v_scale)]
+    st = _lib.adam_step_q8v(ctypes.byref(lst), *[ctypes.cast(p, _PP) for p in ptrs], step,
+                            ctypes.byref(_hp(lr, beta1, beta2, eps, weight_decay)),
+                            ctypes.byref(_q8(stochastic_rounding, seed, percentile, block_size)),
+                            _stream_handle(stream, params))
+    _raise(st, "adam_step_q8v")
+
+
 def q8_quantize(m, v, m_code, v_code, m_scale, v_scale, step: int = 1, stochastic_rounding: bool = False,
                 seed: int = 42, percentile: float = 100.0, block_size: int = BLOCK, stream=None) -> None:
     """Encode fp32 moments into 8-bit codes and block scales (as the step encodes m', v')."""
@@ -238,7 +258,8 @@ def q8_dequantize(m_code, v_code, m_scale, v_scale, m, v, stream=None) -> None:
 # ------------------------------------------------------------------ state allocation (caller side)
 def zeros_state(params, mode: str):
     """Fresh (all-zero) optimizer state for ``params`` in moment mode ``mode``.
-    fp32/bf16m: (m list, v list); q8: (m_code, v_code, m_scale, v_scale) lists."""
+    fp32/bf16m: (m list, v list); q8: (m_code, v_code, m_scale, v_scale) lists;
+    q8v: (m fp32, v_code, v_scale) lists."""
     if mode == "fp32":
         return [torch.zeros_like(p) for p in params], [torch.zeros_like(p) for p in params]
     if mode == "bf16m":
@@ -248,6 +269,10 @@ def zeros_state(params, mode: str):
         return ([torch.zeros(p.numel(), dtype=torch.int8, device=p.device) for p in params],
                 [torch.zeros(p.numel(), dtype=torch.uint8, device=p.device) for p in params],
                 [torch.zeros(n_blocks(p.numel()), dtype=torch.float32, device=p.device) for p in params],
+                [torch.zeros(n_blocks(p.numel()), dtype=torch.float32, device=p.device) for p in params])
+    if mode == "q8v":
+        return ([torch.zeros_like(p) for p in params],
+                [torch.zeros(p.numel(), dtype=torch.uint8, device=p.device) for p in params],
                 [torch.zeros(n_blocks(p.numel()), dtype=torch.float32, device=p.device) for p in params])
     raise ValueError(f"unknown moment mode {mode!r}")
 
@@ -260,6 +285,8 @@ def adam_step(mode: str, params, grads, state, step: int, **kw) -> None:
         adam_step_bf16m(params, grads, *state, step, **kw)
     elif mode == "q8":
         adam_step_q8(params, grads, *state, step, **kw)
+    elif mode == "q8v":
+        adam_step_q8v(params, grads, *state, step, **kw)
     else:
         raise ValueError(f"unknown moment mode {mode!r}")
 
@@ -289,11 +316,15 @@ class StepPlan:
         elif mode == "bf16m":
             _check_layout("m", state[0], torch.bfloat16, params)
             _check_layout("v", state[1], torch.bfloat16, params)
-        else:
+        elif mode == "q8":
             _check_layout("m_code", state[0], torch.int8, params)
             _check_layout("v_code", state[1], torch.uint8, params)
             _check_layout("m_scale", state[2], torch.float32, params, n_blocks)
             _check_layout("v_scale", state[3], torch.float32, params, n_blocks)
+        else:
+            _check_layout("m", state[0], torch.float32, params)
+            _check_layout("v_code", state[1], torch.uint8, params)
+            _check_layout("v_scale", state[2], torch.float32, params, n_blocks)
         self._state_ptrs = [_ptrs(x) for x in state]
         self._state_pp = [ctypes.cast(p, _PP) for p in self._state_ptrs]
         self._state = state
@@ -314,9 +345,12 @@ class StepPlan:
             st = _lib.adam_step_fp32(ctypes.byref(self._lst), *self._state_pp, step, ctypes.byref(self._hp), h)
         elif self.mode == "bf16m":
             st = _lib.adam_step_bf16m(ctypes.byref(self._lst), *self._state_pp, step, ctypes.byref(self._hp), h)
-        else:
+        elif self.mode == "q8":
             st = _lib.adam_step_q8(ctypes.byref(self._lst), *self._state_pp, step, ctypes.byref(self._hp),
                                    ctypes.byref(self._q8), h)
+        else:
+            st = _lib.adam_step_q8v(ctypes.byref(self._lst), *self._state_pp, step, ctypes.byref(self._hp),
+                                    ctypes.byref(self._q8), h)
         _raise(st, f"StepPlan.step ({self.mode})")
 
 

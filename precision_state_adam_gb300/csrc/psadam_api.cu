@@ -156,15 +156,19 @@ template <int CAP>
 Launcher<CAP> pick_step(int mode, bool gb, bool sr, int K) {
   if (mode == kModeF32) return gb ? PSADAM_STEP_FN(kModeF32, true, false, 1, CAP) : PSADAM_STEP_FN(kModeF32, false, false, 1, CAP);
   if (mode == kModeBF16) return gb ? PSADAM_STEP_FN(kModeBF16, true, false, 1, CAP) : PSADAM_STEP_FN(kModeBF16, false, false, 1, CAP);
-#define PSADAM_PICK_K(GB, SR)                                         \
-  if (K == 1) return PSADAM_STEP_FN(kModeQ8, GB, SR, 1, CAP);         \
-  if (K == 4) return PSADAM_STEP_FN(kModeQ8, GB, SR, 4, CAP);         \
-  return PSADAM_STEP_FN(kModeQ8, GB, SR, 16, CAP);
-  if (gb) {
-    if (sr) { PSADAM_PICK_K(true, true) } else { PSADAM_PICK_K(true, false) }
-  } else {
-    if (sr) { PSADAM_PICK_K(false, true) } else { PSADAM_PICK_K(false, false) }
+#define PSADAM_PICK_K(MODE, GB, SR)                                 \
+  if (K == 1) return PSADAM_STEP_FN(MODE, GB, SR, 1, CAP);          \
+  if (K == 4) return PSADAM_STEP_FN(MODE, GB, SR, 4, CAP);          \
+  return PSADAM_STEP_FN(MODE, GB, SR, 16, CAP);
+#define PSADAM_PICK_MODE(MODE)                                      \
+  if (gb) {                                                         \
+    if (sr) { PSADAM_PICK_K(MODE, true, true) } else { PSADAM_PICK_K(MODE, true, false) } \
+  } else {                                                          \
+    if (sr) { PSADAM_PICK_K(MODE, false, true) } else { PSADAM_PICK_K(MODE, false, false) } \
   }
+  if (mode == kModeQ8V) { PSADAM_PICK_MODE(kModeQ8V) }
+  PSADAM_PICK_MODE(kModeQ8)
+#undef PSADAM_PICK_MODE
 #undef PSADAM_PICK_K
 }
 
@@ -182,23 +186,26 @@ int dispatch(const std::vector<Entry>& es, const StepConsts& c, uint64_t seed, i
   return run_launches<kCapLarge>(es, c, seed, step, pct, large, stream);
 }
 
-// Shared front half of the three step entry points.
+// Shared front half of the step entry points. need_ms / need_vs: the mode keeps 8-bit m / v
+// codes and so needs their scale arrays.
 int collect_list(const psadam_list* list, const void* const* m, const void* const* v, const float* const* ms,
-                 const float* const* vs, bool q8, std::vector<Entry>& out) {
+                 const float* const* vs, bool need_ms, bool need_vs, std::vector<Entry>& out) {
   if (!list || list->n_tensors < 0) return PSADAM_ERR_INVALID_ARG;
   if (list->n_tensors == 0) return PSADAM_OK;
   if (list->grad_dtype != PSADAM_GRAD_F32 && list->grad_dtype != PSADAM_GRAD_BF16) return PSADAM_ERR_INVALID_ARG;
-  if (!list->numel || !list->param || !list->grad || !m || !v || (q8 && (!ms || !vs)))
+  if (!list->numel || !list->param || !list->grad || !m || !v || (need_ms && !ms) || (need_vs && !vs))
     return PSADAM_ERR_INVALID_ARG;
   out.reserve(list->n_tensors);
   for (int i = 0; i < list->n_tensors; ++i) {
     const long long n = list->numel[i];
-    const int st = q8 ? check_tensor(n, {list->param[i], list->grad[i], m[i], v[i], ms[i], vs[i]})
-                      : check_tensor(n, {list->param[i], list->grad[i], m[i], v[i]});
+    const int st = need_ms ? check_tensor(n, {list->param[i], list->grad[i], m[i], v[i], ms[i], vs[i]})
+                   : need_vs ? check_tensor(n, {list->param[i], list->grad[i], m[i], v[i], vs[i]})
+                             : check_tensor(n, {list->param[i], list->grad[i], m[i], v[i]});
     if (st != PSADAM_OK) return st;
     if (n == 0) continue;
     out.push_back(Entry{list->param[i], list->grad[i], const_cast<void*>(m[i]), const_cast<void*>(v[i]),
-                        q8 ? const_cast<float*>(ms[i]) : nullptr, q8 ? const_cast<float*>(vs[i]) : nullptr, n, i});
+                        need_ms ? const_cast<float*>(ms[i]) : nullptr, need_vs ? const_cast<float*>(vs[i]) : nullptr,
+                        n, i});
   }
   return PSADAM_OK;
 }
@@ -210,12 +217,13 @@ int step_common(int mode, const psadam_list* list, const void* const* m, const v
   if (list->n_tensors == 0) return PSADAM_OK;
   int st = check_hparams(hp, step);
   if (st != PSADAM_OK) return st;
-  if (mode == kModeQ8 && (st = check_q8(q8)) != PSADAM_OK) return st;
+  const bool q8mode = mode == kModeQ8 || mode == kModeQ8V;
+  if (q8mode && (st = check_q8(q8)) != PSADAM_OK) return st;
   std::vector<Entry> es;
-  if ((st = collect_list(list, m, v, ms, vs, mode == kModeQ8, es)) != PSADAM_OK) return st;
-  const float pct = mode == kModeQ8 ? q8->percentile : 100.f;
-  const bool sr = mode == kModeQ8 && q8->stochastic_rounding;
-  const uint64_t seed = mode == kModeQ8 ? q8->seed : 0;
+  if ((st = collect_list(list, m, v, ms, vs, mode == kModeQ8, q8mode, es)) != PSADAM_OK) return st;
+  const float pct = q8mode ? q8->percentile : 100.f;
+  const bool sr = q8mode && q8->stochastic_rounding;
+  const uint64_t seed = q8mode ? q8->seed : 0;
   const int kmax = max_rank(es, pct);
   if (kmax > kMaxRank) return PSADAM_ERR_UNSUPPORTED;
   const int K = rank_template(kmax);
@@ -246,6 +254,12 @@ int adam_step_q8(const psadam_list* list, int8_t* const* m_code, uint8_t* const*
                  void* stream) {
   return step_common(kModeQ8, list, reinterpret_cast<const void* const*>(m_code),
                      reinterpret_cast<const void* const*>(v_code), m_scale, v_scale, step, hp, q8, stream);
+}
+
+int adam_step_q8v(const psadam_list* list, float* const* m, uint8_t* const* v_code, float* const* v_scale,
+                  int64_t step, const psadam_hparams* hp, const psadam_q8_opts* q8, void* stream) {
+  return step_common(kModeQ8V, list, reinterpret_cast<const void* const*>(m),
+                     reinterpret_cast<const void* const*>(v_code), nullptr, v_scale, step, hp, q8, stream);
 }
 
 int psadam_q8_quantize(int32_t n_tensors, const int64_t* numel, const float* const* m, const float* const* v,
@@ -298,6 +312,7 @@ size_t psadam_state_bytes(int32_t mode, int64_t numel) {
     case 0: return 8 * n;
     case 1: return 4 * n;
     case 2: return 2 * n + 8 * (size_t)n_blocks(numel);
+    case 3: return 5 * n + 4 * (size_t)n_blocks(numel);
     default: return 0;
   }
 }

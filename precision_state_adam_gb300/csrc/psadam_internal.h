@@ -19,7 +19,7 @@ constexpr int kCapSmall = 8;
 constexpr int kCapLarge = 440;
 constexpr int kMaxRank = 16;  // largest percentile rank k the 8-bit kernels select
 
-enum Mode : int { kModeF32 = 0, kModeBF16 = 1, kModeQ8 = 2 };
+enum Mode : int { kModeF32 = 0, kModeBF16 = 1, kModeQ8 = 2, kModeQ8V = 3 };  // Q8V: fp32 m, 8-bit v
 
 // Per-step fp32 constants (formed in double on the host, rounded once).
 struct StepConsts {

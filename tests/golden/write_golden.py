@@ -24,6 +24,8 @@ CASES = {
     "q8_rne_n4100": dict(mode="q8", n=4100, steps=4, hp=HParams(), q8=Q8Opts()),
     "q8_sr_p999_n4100": dict(mode="q8", n=4100, steps=4, hp=HParams(weight_decay=0.1),
                              q8=Q8Opts(stochastic_rounding=True, seed=42, percentile=99.9)),
+    "q8v_sr_n3000": dict(mode="q8v", n=3000, steps=4, hp=HParams(weight_decay=0.01),
+                         q8=Q8Opts(stochastic_rounding=True, seed=7, percentile=100.0)),
 }
 
 
@@ -44,6 +46,8 @@ def run(case):
         st = [np.zeros(n, np.float32), np.zeros(n, np.float32)]
     elif mode == "bf16m":
         st = [np.zeros(n, np.uint16), np.zeros(n, np.uint16)]
+    elif mode == "q8v":
+        st = [np.zeros(n, np.float32), np.zeros(n, np.uint8), np.zeros(nb, np.float32)]
     else:
         st = [np.zeros(n, np.int8), np.zeros(n, np.uint8), np.zeros(nb, np.float32), np.zeros(nb, np.float32)]
     for t in range(1, steps + 1):

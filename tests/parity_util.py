@@ -59,6 +59,9 @@ def host_state(mode: str, sizes):
         return [(np.zeros(n, np.float32), np.zeros(n, np.float32)) for n in sizes]
     if mode == "bf16m":
         return [(np.zeros(n, np.uint16), np.zeros(n, np.uint16)) for n in sizes]
+    if mode == "q8v":
+        return [(np.zeros(n, np.float32), np.zeros(n, np.uint8), np.zeros(oracle.n_blocks(n), np.float32))
+                for n in sizes]
     return [(np.zeros(n, np.int8), np.zeros(n, np.uint8), np.zeros(oracle.n_blocks(n), np.float32),
              np.zeros(oracle.n_blocks(n), np.float32)) for n in sizes]
 
@@ -82,6 +85,14 @@ def compare_state(mode: str, got, want, what: str):
         wv = (want[1].astype(np.uint32) << 16).view(np.float32)
         assert_moment(gm, wm, what + " m")
         assert_moment(gv, wv, what + " v")
+    elif mode == "q8v":
+        assert_moment(got[0], want[0], what + " m")
+        assert_codes(got[1], want[1], what + " v codes")
+        assert_moment(got[2], want[2], what + " v scales")
+        same = got[1] == want[1]
+        gv = got[1].astype(np.float32) * np.repeat(got[2], 2048)[: got[1].size]
+        wv = want[1].astype(np.float32) * np.repeat(want[2], 2048)[: want[1].size]
+        assert_moment(gv[same], wv[same], what + " v (dequantized)")
     else:
         assert_codes(got[0], want[0], what + " m codes")
         assert_codes(got[1], want[1], what + " v codes")

@@ -29,7 +29,7 @@ def declared_functions():
 
 def test_header_declares_the_step_entry_points():
     names = declared_functions()
-    for want in ("adam_step_fp32", "adam_step_bf16m", "adam_step_q8", "psadam_q8_quantize",
+    for want in ("adam_step_fp32", "adam_step_bf16m", "adam_step_q8", "adam_step_q8v", "psadam_q8_quantize",
                  "psadam_q8_dequantize", "psadam_state_bytes", "psadam_status_string"):
         assert want in names
 
@@ -52,7 +52,8 @@ def test_state_bytes_closed_form(psa):
         assert lib.psadam_state_bytes(0, n) == 8 * n
         assert lib.psadam_state_bytes(1, n) == 4 * n
         assert lib.psadam_state_bytes(2, n) == 2 * n + 8 * nb
-    assert lib.psadam_state_bytes(3, 10) == 0 and lib.psadam_state_bytes(0, -1) == 0
+        assert lib.psadam_state_bytes(3, n) == 5 * n + 4 * nb
+    assert lib.psadam_state_bytes(4, 10) == 0 and lib.psadam_state_bytes(0, -1) == 0
     n = 1 << 24
     assert 3.99 < lib.psadam_state_bytes(0, n) / lib.psadam_state_bytes(2, n) < 4.0
 

@@ -71,7 +71,7 @@ def run_both(psa, mode, sizes, steps, hp, q8=Q8Opts(), grad_dtype="f32", grad_ki
         g_host = [workloads.to_bf16_bits_truncate(g) for g in g32] if grad_dtype == "bf16" else g32
         grads = _to_dev(g_host)
         kw = hp_kwargs(hp)
-        if mode == "q8":
+        if mode in ("q8", "q8v"):
             kw.update(q8_kwargs(q8))
         psa.adam_step(mode, params, grads, state, t, **kw)
         oracle.step_list(mode, p_host, g_host, ostate, t, hp, q8)
@@ -109,20 +109,21 @@ Q8_CASES = {
 }
 
 
+@pytest.mark.parametrize("mode", ["q8", "q8v"])
 @pytest.mark.parametrize("grad_dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("case", sorted(Q8_CASES))
-def test_q8_step_ragged_list(psa, case, grad_dtype):
+def test_q8_step_ragged_list(psa, case, grad_dtype, mode):
     hp = HParams(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.1)
-    got_p, want_p, got_s, want_s = run_both(psa, "q8", RAGGED, 5, hp, Q8_CASES[case], grad_dtype=grad_dtype,
+    got_p, want_p, got_s, want_s = run_both(psa, mode, RAGGED, 5, hp, Q8_CASES[case], grad_dtype=grad_dtype,
                                             grad_kind="student_t_outliers", grad_std=1e-3)
-    ex = check_all("q8", got_p, want_p, got_s, want_s, f"q8/{case}/{grad_dtype}")
+    ex = check_all(mode, got_p, want_p, got_s, want_s, f"{mode}/{case}/{grad_dtype}")
     assert ex == 1.0, f"expected bit-identical results, exact fraction {ex}"
 
 
 def test_zero_grads_are_pure_decay(psa):
     n = 10000
     p0 = workloads.init_params_np([workloads.TensorSpec("w", (n,))], seed=8)[0]
-    for mode in ("fp32", "bf16m", "q8"):
+    for mode in ("fp32", "bf16m", "q8", "q8v"):
         params = _to_dev([p0])
         state = psa.zeros_state(params, mode)
         want = p0.copy()
@@ -312,6 +313,8 @@ def sampled_run(psa, w: workloads.Workload, mode: str, steps: int, tensor_stride
             st = [np.zeros(ln, np.float32), np.zeros(ln, np.float32)]
         elif mode == "bf16m":
             st = [np.zeros(ln, np.uint16), np.zeros(ln, np.uint16)]
+        elif mode == "q8v":
+            st = [np.zeros(ln, np.float32), np.zeros(ln, np.uint8), np.zeros(1, np.float32)]
         else:
             st = [np.zeros(ln, np.int8), np.zeros(ln, np.uint8), np.zeros(1, np.float32), np.zeros(1, np.float32)]
         host[(i, b)] = (p, st)
@@ -320,7 +323,7 @@ def sampled_run(psa, w: workloads.Workload, mode: str, steps: int, tensor_stride
     for t in range(1, steps + 1):
         workloads.grads_torch(sizes, t, w.grad_std, dev, kind=w.grad_kind, dtype=w.grad_dtype, out=gbuf)
         kw = hp_kwargs(hp)
-        if mode == "q8":
+        if mode in ("q8", "q8v"):
             kw.update(q8_kwargs(q8))
         psa.adam_step(mode, params, gbuf, state, t, **kw)
         for (i, b, lo, ln) in picks:
@@ -331,6 +334,8 @@ def sampled_run(psa, w: workloads.Workload, mode: str, steps: int, tensor_stride
                 oracle.step_fp32(p, g, *st, t, hp)
             elif mode == "bf16m":
                 oracle.step_bf16m(p, g, *st, t, hp)
+            elif mode == "q8v":
+                oracle.step_q8v_block(p, g, *st, t, hp, q8, tensor_idx=i, elem0=lo)
             else:
                 oracle.step_q8_block(p, g, *st, t, hp, q8, tensor_idx=i, elem0=lo)
     torch.cuda.synchronize()
@@ -341,6 +346,9 @@ def sampled_run(psa, w: workloads.Workload, mode: str, steps: int, tensor_stride
         if mode == "q8":
             got_s = (state[0][i][lo:lo + ln].cpu().numpy(), state[1][i][lo:lo + ln].cpu().numpy(),
                      state[2][i][b:b + 1].cpu().numpy(), state[3][i][b:b + 1].cpu().numpy())
+        elif mode == "q8v":
+            got_s = (state[0][i][lo:lo + ln].cpu().numpy(), state[1][i][lo:lo + ln].cpu().numpy(),
+                     state[2][i][b:b + 1].cpu().numpy())
         elif mode == "bf16m":
             got_s = (bf16_bits(state[0][i][lo:lo + ln]), bf16_bits(state[1][i][lo:lo + ln]))
         else:
@@ -355,7 +363,7 @@ def sampled_run(psa, w: workloads.Workload, mode: str, steps: int, tensor_stride
 
 def test_vit_base_list_sampled(psa):
     w = workloads.WORKLOADS["vit_base"]
-    for mode in ("bf16m", "fp32", "q8"):
+    for mode in ("bf16m", "fp32", "q8", "q8v"):
         exact, n = sampled_run(psa, w, mode, steps=w.steps if mode == "bf16m" else 10, tensor_stride=2)
         assert exact == 1.0 and n > 90
 
@@ -366,7 +374,7 @@ def test_flat_1g_heavy_tail_sr_sampled(psa):
     assert exact == 1.0 and n > 2000
 
 
-@pytest.mark.parametrize("mode", ["fp32", "bf16m", "q8"])
+@pytest.mark.parametrize("mode", ["fp32", "bf16m", "q8", "q8v"])
 def test_gpt_1p3b_bf16_grads_sampled(psa, mode):
     w = workloads.WORKLOADS["gpt_1p3b"]
     exact, n = sampled_run(psa, w, mode, steps=w.steps, tensor_stride=5)
@@ -379,14 +387,14 @@ def test_step_plan_matches_direct_calls(psa):
     specs = [workloads.TensorSpec(f"t{i}", (n,)) for i, n in enumerate(sizes)]
     p0 = workloads.init_params_np(specs, seed=17)
     q8 = Q8Opts(True, 3, 99.9)
-    for mode in ("fp32", "bf16m", "q8"):
+    for mode in ("fp32", "bf16m", "q8", "q8v"):
         runs = []
         for use_plan in (False, True):
             params = _to_dev(p0)
             state = psa.zeros_state(params, mode)
             gbufs = [_to_dev(workloads.grads_np(sizes, t, 1e-2, seed=17)) for t in (1, 2, 3)]
             kw = dict(weight_decay=0.01)
-            if mode == "q8":
+            if mode in ("q8", "q8v"):
                 kw.update(q8_kwargs(q8))
             if use_plan:
                 plan = psa.StepPlan(mode, params, gbufs[0], state, **kw)

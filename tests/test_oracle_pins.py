@@ -465,3 +465,48 @@ def test_state_memory_ratio():
     fp32_bytes = 2 * 4 * n
     q8_bytes = 2 * n + 2 * 4 * oracle.n_blocks(n)
     assert 3.99 < fp32_bytes / q8_bytes < 4.0
+
+
+def test_q8v_keeps_m_exact_and_quantizes_v_only():
+    """CompressBothMoments = false (PR #814): m stays fp32, so p and m follow the fp32-moment
+    step bit for bit when v's quantization is lossless; from zero state they always do at
+    t = 1, and v's codes are v' quantized as the unsigned channel of an 8-bit block."""
+    hp = HParams(weight_decay=0.01)
+    n = 2048 * 2 + 300
+    p, g = _fresh(n, seed=21)
+    pf, mf, vf = p.copy(), np.zeros_like(p), np.zeros_like(p)
+    oracle.step_fp32(pf, g, mf, vf, 1, hp)
+    nb = oracle.n_blocks(n)
+    pq, mq, vc, vs = p.copy(), np.zeros_like(p), np.zeros(n, np.uint8), np.zeros(nb, F32)
+    oracle.step_q8v(pq, g, mq, vc, vs, 1, hp)
+    np.testing.assert_array_equal(pq, pf)
+    np.testing.assert_array_equal(mq, mf)
+    for b in range(nb):
+        lo, hi = b * 2048, min(n, (b + 1) * 2048)
+        codes, s = oracle.quantize_block(vf[lo:hi], False)
+        np.testing.assert_array_equal(vc[lo:hi], codes)
+        assert vs[b] == s
+    # a second step: m is never quantized, so it equals the textbook recursion on the same g
+    _, g2 = _fresh(n, seed=22)
+    m_expect = (F32(0.9) * mq + F32(np.float32(1.0 - np.float64(F32(0.9)))) * g2).astype(F32)
+    oracle.step_q8v(pq, g2, mq, vc, vs, 2, hp)
+    np.testing.assert_array_equal(mq, m_expect)
+
+
+def test_q8v_block_equals_range_step():
+    hp = HParams(weight_decay=0.1)
+    n = 2048 * 3 + 11
+    p, g = _fresh(n, seed=23)
+    nb = oracle.n_blocks(n)
+    a = [p.copy(), np.zeros_like(p), np.zeros(n, np.uint8), np.zeros(nb, F32)]
+    b = [x.copy() for x in a]
+    q8 = Q8Opts(True, 9, 99.9)
+    for t in (1, 2):
+        oracle.step_q8v(a[0], g, a[1], a[2], a[3], t, hp, q8, tensor_idx=3)
+        for blk in range(nb):
+            lo, hi = blk * 2048, min(n, (blk + 1) * 2048)
+            sub = [b[0][lo:hi].copy(), b[1][lo:hi].copy(), b[2][lo:hi].copy(), b[3][blk:blk + 1].copy()]
+            oracle.step_q8v_block(sub[0], g[lo:hi].copy(), sub[1], sub[2], sub[3], t, hp, q8, 3, lo)
+            b[0][lo:hi], b[1][lo:hi], b[2][lo:hi], b[3][blk] = sub[0], sub[1], sub[2], sub[3][0]
+    for x, y in zip(a, b):
+        np.testing.assert_array_equal(x, y)
