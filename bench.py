@@ -43,12 +43,13 @@ L2_FLUSH_BYTES = 384 << 20
 STATE_BYTES = {"fp32": (4, 4), "bf16m": (2, 2), "q8": (1, 1), "q8v": (4, 1)}   # per m, v element
 
 
-def algorithmic_bytes(mode: str, sizes, grad_dtype: str) -> int:
-    """Bytes the step must move once each: p read+write, g read, m and v read+write,
-    and for 8-bit moments the two fp32 scales of every block read+write."""
+def algorithmic_bytes(mode: str, sizes, grad_dtype: str, zero_grads: bool = False) -> int:
+    """Bytes the step must move once each: p read+write, g read (and written with zeros
+    when zero_grads), m and v read+write, and for 8-bit moments the fp32 scales of every
+    block read+write."""
     g = 4 if grad_dtype == "f32" else 2
     mb, vb = STATE_BYTES[mode]
-    per = 8 + g + 2 * mb + 2 * vb
+    per = 8 + g * (2 if zero_grads else 1) + 2 * mb + 2 * vb
     total = per * sum(sizes)
     scales = {"q8": 2, "q8v": 1}.get(mode, 0)  # fp32 scale arrays, read + written per block
     total += 8 * scales * sum((n + 2047) // 2048 for n in sizes)
@@ -185,6 +186,8 @@ def run_ours(args, rank: int, world: int, dist):
         kw = dict(lr=w.lr, beta1=w.beta1, beta2=w.beta2, eps=w.eps, weight_decay=w.weight_decay)
         if mode in ("q8", "q8v"):
             kw.update(stochastic_rounding=w.stochastic_rounding, seed=w.seed, percentile=w.percentile)
+        if args.zero_grads:
+            kw.update(zero_grads=True)
         launches_per_step = -(-len([n for n in sizes if n > 0]) // (8 if len(sizes) <= 8 else 440))
         # one marshalled plan per grad set: a step is then a single C call
         plans = [psa.StepPlan(mode, params, grads[s], state, **kw) for s in range(n_sets)]
@@ -211,7 +214,7 @@ def run_ours(args, rank: int, world: int, dist):
             dist.barrier()
         step_ms = [a.elapsed_time(b) for a, b in evs]
         total_s = max_over_ranks(sum(step_ms) / 1e3, dist, dev)
-        nbytes = algorithmic_bytes(mode, sizes, w.grad_dtype)
+        nbytes = algorithmic_bytes(mode, sizes, w.grad_dtype, args.zero_grads)
         mean_s = sum(step_ms) / len(step_ms) / 1e3
         results[mode] = {
             "gparams_per_s": job_gparams_per_s(numel, args.steps, total_s, world),
@@ -344,6 +347,8 @@ def main():
     ap.add_argument("--modes", default=None, help="comma list; the first is the headline (default: workload's)")
     ap.add_argument("--numel", type=int, default=None,
                     help="resize a one-tensor workload (for profiling small cases)")
+    ap.add_argument("--zero-grads", action="store_true",
+                    help="zero the grads inside the step (adds a grad write per param)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-step-seconds", type=float, default=3.0)
@@ -398,6 +403,7 @@ def main():
                        "params": sum(w.sizes), "tensors": len(w.sizes), "grad_dtype": w.grad_dtype,
                        "bytes_per_step": r["bytes_per_step"],
                        "l2": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MB write outside the step events)",
+                       "zero_grads": bool(args.zero_grads),
                        "grads": "8 seeded sets resident in HBM, cycled"},
             "roofline": {"bound": "hbm", "achieved": round(r["achieved_gbs"], 1), "peak": peak, "unit": "GB/s",
                          "frac": round(r["achieved_gbs"] / peak, 4), "peak_kind": peak_kind,

@@ -94,13 +94,23 @@ typedef struct {
                                     (percentile >= ~99.27 for full blocks), else UNSUPPORTED */
 } psadam_q8_opts;
 
-/* The parameter/gradient side of a multi-tensor list. */
+/* The parameter/gradient side of a multi-tensor list, with the grad-side work that sits on
+ * either side of the update in a mixed-precision training step. A zero-initialised tail
+ * (grad_unscale 0, zero_grads 0, skip_if_set NULL) changes nothing. */
 typedef struct {
     int32_t n_tensors;
     int32_t grad_dtype;          /* psadam_grad_dtype: fp32 or bf16 grads (widened exactly) */
     const int64_t* numel;        /* host [n_tensors] element counts */
     float* const* param;         /* host [n_tensors] device fp32 params, updated in place */
-    const void* const* grad;     /* host [n_tensors] device grads (float* or bf16 bits), read only */
+    const void* const* grad;     /* host [n_tensors] device grads (float* or bf16 bits); read, and
+                                    written only when zero_grads != 0 */
+    float grad_unscale;          /* each grad is multiplied by this (one fp32 rounding) before use,
+                                    e.g. 1/loss_scale; 0 reads as 1. Must be finite. */
+    int32_t zero_grads;          /* nonzero: every grad is overwritten with 0 after it is read
+                                    (adds 4 bytes/param of writes, 2 for bf16 grads) */
+    const int32_t* skip_if_set;  /* device int32 or NULL: when it holds a nonzero value at launch
+                                    the step changes nothing (e.g. psadam_check_grads found an
+                                    inf/NaN). 4-byte aligned. */
 } psadam_list;
 
 /* One AdamW step with fp32 moments. m, v: host [n_tensors] of device float[numel],
@@ -147,6 +157,12 @@ int psadam_q8_dequantize(int32_t n_tensors, const int64_t* numel, const int8_t* 
                          const uint8_t* const* v_code, const float* const* m_scale,
                          const float* const* v_scale, float* const* m, float* const* v,
                          void* stream);
+
+/* Non-finite grad check (the "found inf" test of a mixed-precision step): writes 0 to the
+ * device int32 *found_nonfinite, then 1 if any grad of the list, multiplied by
+ * list->grad_unscale, is +-inf or NaN. Only the grad side of `list` is used (param may be
+ * NULL). Pass the same flag as skip_if_set of the following step to skip it. */
+int psadam_check_grads(const psadam_list* list, int32_t* found_nonfinite, void* stream);
 
 /* Bytes of optimizer state for a tensor of numel params (PR #814's GetMemoryUsage):
  * mode 0 = fp32 (8*numel), 1 = bf16 (4*numel), 2 = 8-bit (2*numel + 8*ceil(numel/2048)),

@@ -93,6 +93,7 @@ def _load() -> ctypes.CDLL:
         "orc_step_q8_block": (None, [i64, i64, _f32p, vp, i32, _i8p, _u8p, _f32p, _f32p, hp, i64, q8, i32]),
         "orc_step_q8v": (None, [i64, _f32p, vp, i32, _f32p, _u8p, _f32p, hp, i64, q8, i32, i64, i64]),
         "orc_step_q8v_block": (None, [i64, i64, _f32p, vp, i32, _f32p, _u8p, _f32p, hp, i64, q8, i32]),
+        "orc_unscale_grads": (None, [i64, vp, i32, ctypes.c_float, _f32p]),
         "orc_probe_mul_add": (ctypes.c_float, [ctypes.c_float] * 3),
     }
     for name, (res, args) in sigs.items():
@@ -316,6 +317,15 @@ def step_list(mode: str, params, grads, state, t: int, hp: HParams, q8: Q8Opts =
             step_q8v(p, g, *st, t, hp, q8, tensor_idx=i)
         else:
             raise ValueError(mode)
+
+
+def unscale_grads(g: np.ndarray, unscale: float) -> np.ndarray:
+    """The grads the update sees: g * unscale in fp32 (bf16 bits widened first)."""
+    n = g.size
+    gp, gb = _grad(g, n)
+    out = np.empty(n, np.float32)
+    _lib.orc_unscale_grads(n, gp, gb, unscale, _ptr(out, ctypes.c_float))
+    return out
 
 
 def probe_mul_add(a: float, b: float, c: float) -> np.float32:

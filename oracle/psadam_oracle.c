@@ -336,4 +336,11 @@ void orc_step_q8v(int64_t n, float* p, const void* grad, int grad_bf16, float* m
     }
 }
 
+/* Grad side of a mixed-precision step (the pages are silent; the plain reading of loss
+ * scaling): each grad is multiplied by the inverse loss scale, one fp32 rounding, before
+ * the update sees it. bf16 grads are widened first (exactly). */
+void orc_unscale_grads(int64_t n, const void* grad, int grad_bf16, float unscale, float* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = load_grad(grad, grad_bf16, i) * unscale;
+}
+
 float orc_probe_mul_add(float a, float b, float c) { return a * b + c; }

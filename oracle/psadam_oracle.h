@@ -111,6 +111,9 @@ void orc_step_q8v_block(int64_t cnt, int64_t elem0, float* p, const void* grad, 
                         uint8_t* v_code, float* v_scale, const orc_hparams* hp, int64_t t,
                         const orc_q8opts* q, int tensor_idx);
 
+/* out[i] = grad[i] * unscale (one fp32 rounding; bf16 grads widened first). */
+void orc_unscale_grads(int64_t n, const void* grad, int grad_bf16, float unscale, float* out);
+
 /* Build-flag probe: returns a*b + c with two roundings. A build that let the
  * compiler contract this into one fused multiply-add would return the fused value. */
 float orc_probe_mul_add(float a, float b, float c);

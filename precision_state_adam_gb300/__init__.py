@@ -50,7 +50,8 @@ class _Q8Opts(ctypes.Structure):
 class _List(ctypes.Structure):
     _fields_ = [("n_tensors", ctypes.c_int32), ("grad_dtype", ctypes.c_int32),
                 ("numel", ctypes.POINTER(ctypes.c_int64)), ("param", ctypes.POINTER(ctypes.c_void_p)),
-                ("grad", ctypes.POINTER(ctypes.c_void_p))]
+                ("grad", ctypes.POINTER(ctypes.c_void_p)), ("grad_unscale", ctypes.c_float),
+                ("zero_grads", ctypes.c_int32), ("skip_if_set", ctypes.c_void_p)]
 
 
 _lib = ctypes.CDLL(LIB_PATH)
@@ -67,6 +68,7 @@ _SIGS = {
     "psadam_q8_quantize": [ctypes.c_int32, _I64P, _PP, _PP, _PP, _PP, _PP, _PP, ctypes.POINTER(_Q8Opts),
                            ctypes.c_int64, _vp],
     "psadam_q8_dequantize": [ctypes.c_int32, _I64P, _PP, _PP, _PP, _PP, _PP, _PP, _vp],
+    "psadam_check_grads": [ctypes.POINTER(_List), _vp, _vp],
 }
 for _name, _args in _SIGS.items():
     getattr(_lib, _name).argtypes = _args
@@ -142,17 +144,28 @@ def _hp(lr, beta1, beta2, eps, weight_decay) -> _HParams:
     return _HParams(lr, beta1, beta2, eps, weight_decay)
 
 
-def _list(params, grads):
-    if len(params) != len(grads):
-        raise ValueError("params and grads differ in length")
-    _check_layout("params", params, torch.float32)
+def _skip_ptr(skip_flag) -> int | None:
+    if skip_flag is None:
+        return None
+    if skip_flag.dtype != torch.int32 or not skip_flag.is_cuda or skip_flag.numel() < 1:
+        raise TypeError("skip_flag must be a CUDA int32 tensor")
+    return skip_flag.data_ptr()
+
+
+def _list(params, grads, grad_unscale: float = 1.0, zero_grads: bool = False, skip_flag=None, like=None):
+    if like is None:
+        like = params
+        if len(params) != len(grads):
+            raise ValueError("params and grads differ in length")
+        _check_layout("params", params, torch.float32)
     gdt = grads[0].dtype if grads else torch.float32
     if gdt not in (torch.float32, torch.bfloat16):
         raise TypeError("grads must be float32 or bfloat16")
-    _check_layout("grads", grads, gdt, params)
-    keep = (_numels(params), _ptrs(params), _ptrs(grads))
-    lst = _List(len(params), GRAD_BF16 if gdt == torch.bfloat16 else GRAD_F32, keep[0],
-                ctypes.cast(keep[1], _PP), ctypes.cast(keep[2], _PP))
+    _check_layout("grads", grads, gdt, like)
+    keep = (_numels(like), _ptrs(params) if params is not None else None, _ptrs(grads))
+    lst = _List(len(grads), GRAD_BF16 if gdt == torch.bfloat16 else GRAD_F32, keep[0],
+                ctypes.cast(keep[1], _PP) if keep[1] is not None else None, ctypes.cast(keep[2], _PP),
+                grad_unscale, int(bool(zero_grads)), _skip_ptr(skip_flag))
     return lst, keep
 
 
@@ -163,9 +176,13 @@ def _raise(status: int, where: str) -> None:
 
 # ------------------------------------------------------------------ steps
 def adam_step_fp32(params, grads, m, v, step: int, lr: float = 1e-3, beta1: float = 0.9, beta2: float = 0.999,
-                   eps: float = 1e-8, weight_decay: float = 0.0, stream=None) -> None:
-    """One AdamW step with fp32 moments, in place, enqueued on ``stream`` (default: current)."""
-    lst, keep = _list(params, grads)
+                   eps: float = 1e-8, weight_decay: float = 0.0, grad_unscale: float = 1.0, zero_grads: bool = False,
+                   skip_flag=None, stream=None) -> None:
+    """One AdamW step with fp32 moments, in place, enqueued on ``stream`` (default: current).
+    Grad side: grads are multiplied by ``grad_unscale`` before use, overwritten with zeros
+    after use when ``zero_grads``, and the whole step is skipped on the device when the
+    CUDA int32 tensor ``skip_flag`` holds a nonzero value (see :func:`check_grads`)."""
+    lst, keep = _list(params, grads, grad_unscale, zero_grads, skip_flag)
     _check_layout("m", m, torch.float32, params)
     _check_layout("v", v, torch.float32, params)
     mp, vp = _ptrs(m), _ptrs(v)
@@ -175,9 +192,11 @@ def adam_step_fp32(params, grads, m, v, step: int, lr: float = 1e-3, beta1: floa
 
 
 def adam_step_bf16m(params, grads, m, v, step: int, lr: float = 1e-3, beta1: float = 0.9, beta2: float = 0.999,
-                    eps: float = 1e-8, weight_decay: float = 0.0, stream=None) -> None:
-    """One AdamW step with bf16 moments (torch.bfloat16 tensors), in place."""
-    lst, keep = _list(params, grads)
+                   eps: float = 1e-8, weight_decay: float = 0.0, grad_unscale: float = 1.0, zero_grads: bool = False,
+                   skip_flag=None, stream=None) -> None:
+    """One AdamW step with bf16 moments (torch.bfloat16 tensors), in place (grad-side
+    options as for :func:`adam_step_fp32`)."""
+    lst, keep = _list(params, grads, grad_unscale, zero_grads, skip_flag)
     _check_layout("m", m, torch.bfloat16, params)
     _check_layout("v", v, torch.bfloat16, params)
     mp, vp = _ptrs(m), _ptrs(v)
@@ -192,10 +211,11 @@ def _q8(stochastic_rounding: bool, seed: int, percentile: float, block_size: int
 
 def adam_step_q8(params, grads, m_code, v_code, m_scale, v_scale, step: int, lr: float = 1e-3, beta1: float = 0.9,
                  beta2: float = 0.999, eps: float = 1e-8, weight_decay: float = 0.0, stochastic_rounding: bool = False,
-                 seed: int = 42, percentile: float = 100.0, block_size: int = BLOCK, stream=None) -> None:
+                 seed: int = 42, percentile: float = 100.0, block_size: int = BLOCK, grad_unscale: float = 1.0,
+                 zero_grads: bool = False, skip_flag=None, stream=None) -> None:
     """One AdamW step with 8-bit block-wise moments (int8 m codes, uint8 v codes, fp32
     per-block scales), dequantize-update-requantize in one pass, in place."""
-    lst, keep = _list(params, grads)
+    lst, keep = _list(params, grads, grad_unscale, zero_grads, skip_flag)
     _check_layout("m_code", m_code, torch.int8, params)
     _check_layout("v_code", v_code, torch.uint8, params)
     _check_layout("m_scale", m_scale, torch.float32, params, n_blocks)
@@ -210,10 +230,11 @@ def adam_step_q8(params, grads, m_code, v_code, m_scale, v_scale, step: int, lr:
 
 def adam_step_q8v(params, grads, m, v_code, v_scale, step: int, lr: float = 1e-3, beta1: float = 0.9,
                   beta2: float = 0.999, eps: float = 1e-8, weight_decay: float = 0.0, stochastic_rounding: bool = False,
-                  seed: int = 42, percentile: float = 100.0, block_size: int = BLOCK, stream=None) -> None:
+                  seed: int = 42, percentile: float = 100.0, block_size: int = BLOCK, grad_unscale: float = 1.0,
+                  zero_grads: bool = False, skip_flag=None, stream=None) -> None:
     """One AdamW step with an fp32 first moment and an 8-bit block-wise second moment
     (uint8 v codes, fp32 per-block scales), in place."""
-    lst, keep = _list(params, grads)
+    lst, keep = _list(params, grads, grad_unscale, zero_grads, skip_flag)
     _check_layout("m", m, torch.float32, params)
     _check_layout("v_code", v_code, torch.uint8, params)
     _check_layout("v_scale", v_scale, torch.float32, params, n_blocks)
@@ -223,6 +244,16 @@ def adam_step_q8v(params, grads, m, v_code, v_scale, step: int, lr: float = 1e-3
                             ctypes.byref(_q8(stochastic_rounding, seed, percentile, block_size)),
                             _stream_handle(stream, params))
     _raise(st, "adam_step_q8v")
+
+
+def check_grads(grads, found_nonfinite, grad_unscale: float = 1.0, stream=None) -> None:
+    """Set the CUDA int32 tensor ``found_nonfinite`` to 1 if any grad times ``grad_unscale``
+    is +-inf or NaN, else 0 (enqueued on the stream; pass it as ``skip_flag`` to the step)."""
+    if found_nonfinite.dtype != torch.int32 or not found_nonfinite.is_cuda:
+        raise TypeError("found_nonfinite must be a CUDA int32 tensor")
+    lst, keep = _list(None, grads, grad_unscale, like=grads)
+    st = _lib.psadam_check_grads(ctypes.byref(lst), found_nonfinite.data_ptr(), _stream_handle(stream, grads))
+    _raise(st, "psadam_check_grads")
 
 
 def q8_quantize(m, v, m_code, v_code, m_scale, v_scale, step: int = 1, stochastic_rounding: bool = False,
@@ -303,11 +334,12 @@ class StepPlan:
     def __init__(self, mode: str, params, grads, state, lr: float = 1e-3, beta1: float = 0.9,
                  beta2: float = 0.999, eps: float = 1e-8, weight_decay: float = 0.0,
                  stochastic_rounding: bool = False, seed: int = 42, percentile: float = 100.0,
-                 block_size: int = BLOCK):
+                 block_size: int = BLOCK, grad_unscale: float = 1.0, zero_grads: bool = False, skip_flag=None):
         if mode not in MODES:
             raise ValueError(f"unknown moment mode {mode!r}")
         self.mode = mode
-        self._lst, self._keep = _list(params, grads)
+        self._skip = skip_flag
+        self._lst, self._keep = _list(params, grads, grad_unscale, zero_grads, skip_flag)
         self._grad_dtype = grads[0].dtype if grads else torch.float32
         self._params = list(params)
         if mode == "fp32":

@@ -1,4 +1,5 @@
-// Instantiations: quantize-only and dequantize-only kernels of the 8-bit moment format.
+// Instantiations: quantize-only / dequantize-only kernels of the 8-bit moment format and the
+// non-finite grad check.
 #include "psadam_kernels.cuh"
 
 namespace psadam {
@@ -12,4 +13,8 @@ PSADAM_INST_K(true, kCapLarge)
 #undef PSADAM_INST
 template cudaError_t launch_dequantize<kCapSmall>(const LaunchArgs<kCapSmall>&, cudaStream_t);
 template cudaError_t launch_dequantize<kCapLarge>(const LaunchArgs<kCapLarge>&, cudaStream_t);
+template cudaError_t launch_check_grads<false, kCapSmall>(const LaunchArgs<kCapSmall>&, int*, cudaStream_t);
+template cudaError_t launch_check_grads<true, kCapSmall>(const LaunchArgs<kCapSmall>&, int*, cudaStream_t);
+template cudaError_t launch_check_grads<false, kCapLarge>(const LaunchArgs<kCapLarge>&, int*, cudaStream_t);
+template cudaError_t launch_check_grads<true, kCapLarge>(const LaunchArgs<kCapLarge>&, int*, cudaStream_t);
 }  // namespace psadam

@@ -107,13 +107,23 @@ int max_rank(const std::vector<Entry>& es, float pct) {
 template <int CAP>
 using Launcher = cudaError_t (*)(const LaunchArgs<CAP>&, cudaStream_t);
 
+// Grad-side options of a step (see psadam_list).
+struct GradSide {
+  float unscale = 1.0f;
+  int zero = 0;
+  const int* skip = nullptr;
+};
+
 // Pack the list into as few launches as fit and run `fn` on each.
-template <int CAP>
+template <int CAP, typename Fn>
 int run_launches(const std::vector<Entry>& es, const StepConsts& c, uint64_t seed, int64_t step, float pct,
-                 Launcher<CAP> fn, cudaStream_t stream) {
+                 const GradSide& gs, Fn fn, cudaStream_t stream) {
   static thread_local LaunchArgs<CAP> a;  // ~32 KB: keep it off the stack
   std::memset(&a, 0, sizeof a);
   a.c = c;
+  a.g_unscale = gs.unscale;
+  a.zero_grads = gs.zero;
+  a.skip = gs.skip;
   a.seed_lo = (uint32_t)(seed & 0xFFFFFFFFu);
   a.seed_hi = (uint32_t)(seed >> 32);
   a.step_lo = (uint32_t)step;
@@ -180,10 +190,21 @@ Launcher<CAP> pick_quantize(bool sr, int K) {
 
 // Dispatch on list length: short lists use the small parameter block.
 int dispatch(const std::vector<Entry>& es, const StepConsts& c, uint64_t seed, int64_t step, float pct,
-             Launcher<kCapSmall> small, Launcher<kCapLarge> large, cudaStream_t stream) {
+             Launcher<kCapSmall> small, Launcher<kCapLarge> large, cudaStream_t stream,
+             const GradSide& gs = GradSide{}) {
   if (es.empty()) return PSADAM_OK;
-  if (es.size() <= (size_t)kCapSmall) return run_launches<kCapSmall>(es, c, seed, step, pct, small, stream);
-  return run_launches<kCapLarge>(es, c, seed, step, pct, large, stream);
+  if (es.size() <= (size_t)kCapSmall) return run_launches<kCapSmall>(es, c, seed, step, pct, gs, small, stream);
+  return run_launches<kCapLarge>(es, c, seed, step, pct, gs, large, stream);
+}
+
+// The list's grad-side options; 0 as an unscale factor reads as 1 (a zeroed struct changes nothing).
+int grad_side(const psadam_list* list, GradSide& gs) {
+  gs.unscale = list->grad_unscale == 0.0f ? 1.0f : list->grad_unscale;
+  if (!finite(gs.unscale)) return PSADAM_ERR_INVALID_ARG;
+  gs.zero = list->zero_grads != 0;
+  gs.skip = list->skip_if_set;
+  if (gs.skip && (reinterpret_cast<uintptr_t>(gs.skip) & 3u)) return PSADAM_ERR_MISALIGNED;
+  return PSADAM_OK;
 }
 
 // Shared front half of the step entry points. need_ms / need_vs: the mode keeps 8-bit m / v
@@ -226,11 +247,13 @@ int step_common(int mode, const psadam_list* list, const void* const* m, const v
   const uint64_t seed = q8mode ? q8->seed : 0;
   const int kmax = max_rank(es, pct);
   if (kmax > kMaxRank) return PSADAM_ERR_UNSUPPORTED;
+  GradSide gs;
+  if ((st = grad_side(list, gs)) != PSADAM_OK) return st;
   const int K = rank_template(kmax);
   const bool gb = list->grad_dtype == PSADAM_GRAD_BF16;
   const StepConsts c = make_consts(*hp, step);
   return dispatch(es, c, seed, step, pct, pick_step<kCapSmall>(mode, gb, sr, K), pick_step<kCapLarge>(mode, gb, sr, K),
-                  static_cast<cudaStream_t>(stream));
+                  static_cast<cudaStream_t>(stream), gs);
 }
 
 }  // namespace
@@ -303,6 +326,39 @@ int psadam_q8_dequantize(int32_t n_tensors, const int64_t* numel, const int8_t* 
   }
   return dispatch(es, StepConsts{}, 0, 1, 100.f, &launch_dequantize<kCapSmall>, &launch_dequantize<kCapLarge>,
                   static_cast<cudaStream_t>(stream));
+}
+
+int psadam_check_grads(const psadam_list* list, int32_t* found_nonfinite, void* stream) {
+  if (!list || list->n_tensors < 0 || !found_nonfinite) return PSADAM_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(found_nonfinite) & 3u) return PSADAM_ERR_MISALIGNED;
+  if (list->grad_dtype != PSADAM_GRAD_F32 && list->grad_dtype != PSADAM_GRAD_BF16) return PSADAM_ERR_INVALID_ARG;
+  if (list->n_tensors > 0 && (!list->numel || !list->grad)) return PSADAM_ERR_INVALID_ARG;
+  GradSide gs;
+  int st = grad_side(list, gs);
+  if (st != PSADAM_OK) return st;
+  std::vector<Entry> es;
+  for (int i = 0; i < list->n_tensors; ++i) {
+    if ((st = check_tensor(list->numel[i], {list->grad[i]})) != PSADAM_OK) return st;
+    if (list->numel[i] == 0) continue;
+    es.push_back(Entry{nullptr, list->grad[i], nullptr, nullptr, nullptr, nullptr, list->numel[i], i});
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const cudaError_t e0 = cudaMemsetAsync(found_nonfinite, 0, sizeof(int32_t), s);
+  if (e0 != cudaSuccess) {
+    g_last_cuda_error = (int32_t)e0;
+    return PSADAM_ERR_CUDA;
+  }
+  if (es.empty()) return PSADAM_OK;
+  const bool gb = list->grad_dtype == PSADAM_GRAD_BF16;
+  int* flag = found_nonfinite;
+  auto small = [&](const LaunchArgs<kCapSmall>& a, cudaStream_t ss) {
+    return gb ? launch_check_grads<true, kCapSmall>(a, flag, ss) : launch_check_grads<false, kCapSmall>(a, flag, ss);
+  };
+  auto large = [&](const LaunchArgs<kCapLarge>& a, cudaStream_t ss) {
+    return gb ? launch_check_grads<true, kCapLarge>(a, flag, ss) : launch_check_grads<false, kCapLarge>(a, flag, ss);
+  };
+  if (es.size() <= (size_t)kCapSmall) return run_launches<kCapSmall>(es, StepConsts{}, 0, 1, 100.f, gs, small, s);
+  return run_launches<kCapLarge>(es, StepConsts{}, 0, 1, 100.f, gs, large, s);
 }
 
 size_t psadam_state_bytes(int32_t mode, int64_t numel) {

@@ -50,7 +50,9 @@ struct LaunchArgs {
   int k_full;       // percentile rank of a full 2048-element block
   int n_tensors;
   int total_blocks;
-  int pad_[2];
+  float g_unscale;  // grads are multiplied by this before use (1: unchanged)
+  int zero_grads;   // nonzero: overwrite each grad with zero after reading it
+  const int* skip;  // device flag or null: a nonzero value makes the launch a no-op
   TensorRef t[CAP];
 };
 static_assert(sizeof(LaunchArgs<kCapLarge>) <= 32764, "kernel parameter block too large");
@@ -67,5 +69,9 @@ cudaError_t launch_quantize(const LaunchArgs<CAP>& a, cudaStream_t s);
 
 template <int CAP>
 cudaError_t launch_dequantize(const LaunchArgs<CAP>& a, cudaStream_t s);
+
+// Non-finite grad check: sets *flag = 1 if any grad (times g_unscale) is inf or NaN.
+template <bool GBF16, int CAP>
+cudaError_t launch_check_grads(const LaunchArgs<CAP>& a, int* flag, cudaStream_t s);
 
 }  // namespace psadam

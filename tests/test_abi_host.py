@@ -110,6 +110,24 @@ def test_validation_errors(psa):
     assert _call_q8(psa, numel=((2 ** 31) * 2048,)) == E.ERR_UNSUPPORTED
 
 
+def test_grad_side_validation(psa):
+    import ctypes as C
+    nums = _arr(C.c_int64, [4096])
+    ptrs = _arr(C.c_void_p, [FAKE])
+    P = C.cast(ptrs, psa._PP)
+    hp = psa._HParams(1e-3, 0.9, 0.999, 1e-8, 0.0)
+    q = psa._Q8Opts(2048, 0, 42, 100.0)
+    lib = psa.cdll()
+    for unscale, skip, want in ((float("inf"), None, psa.ERR_INVALID_ARG), (float("nan"), None, psa.ERR_INVALID_ARG),
+                                (1.0, FAKE + 2, psa.ERR_MISALIGNED)):
+        lst = psa._List(1, 0, nums, P, P, unscale, 0, skip)
+        assert lib.adam_step_q8(C.byref(lst), P, P, P, P, 1, C.byref(hp), C.byref(q), None) == want
+    lst = psa._List(1, 0, nums, P, P, 1.0, 0, None)
+    assert lib.psadam_check_grads(C.byref(lst), None, None) == psa.ERR_INVALID_ARG
+    assert lib.psadam_check_grads(C.byref(lst), FAKE + 1, None) == psa.ERR_MISALIGNED
+    assert lib.psadam_check_grads(None, FAKE, None) == psa.ERR_INVALID_ARG
+
+
 def test_percentile_rank_limit_follows_the_block(psa):
     # 99.0 -> rank 21 of a full block: beyond the selectable 16, rejected before launch
     assert _call_q8(psa, numel=(2048,), pct=99.0) == psa.ERR_UNSUPPORTED

@@ -510,3 +510,20 @@ def test_q8v_block_equals_range_step():
             b[0][lo:hi], b[1][lo:hi], b[2][lo:hi], b[3][blk] = sub[0], sub[1], sub[2], sub[3][0]
     for x, y in zip(a, b):
         np.testing.assert_array_equal(x, y)
+
+
+def test_grad_unscale_is_one_rounding_of_the_product():
+    rng = np.random.default_rng(31)
+    g = (rng.standard_normal(5000) * 1e3).astype(F32)
+    # a power-of-two inverse loss scale is exact
+    np.testing.assert_array_equal(oracle.unscale_grads(g, 2.0 ** -10), np.ldexp(g, -10).astype(F32))
+    np.testing.assert_array_equal(oracle.unscale_grads(g, 1.0), g)
+    # otherwise: the product rounded once (float64 product of two floats is exact)
+    u = float(F32(1 / 3))
+    np.testing.assert_array_equal(oracle.unscale_grads(g, u), (g.astype(np.float64) * u).astype(F32))
+    # bf16 grads are widened exactly first
+    gb = workloads.to_bf16_bits_truncate(g)
+    wide = (gb.astype(np.uint32) << 16).view(F32)
+    np.testing.assert_array_equal(oracle.unscale_grads(gb, u), (wide.astype(np.float64) * u).astype(F32))
+    # overflow of the product is an inf the check must catch
+    assert np.isinf(oracle.unscale_grads(np.array([3e38], F32), 10.0)[0])
