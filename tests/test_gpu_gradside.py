@@ -36,6 +36,10 @@ def _dev(arrs):
     return out
 
 
+def _host(x: torch.Tensor) -> np.ndarray:
+    return (x.view(torch.int16) if x.dtype == torch.bfloat16 else x).cpu().numpy()
+
+
 def _grads(step, bf16, scale=1.0, seed=40):
     g = [x * np.float32(scale) for x in workloads.grads_np(SIZES, step, 1e-2, seed=seed)]
     return [workloads.to_bf16_bits_truncate(x) for x in g] if bf16 else [x.astype(np.float32) for x in g]
@@ -97,11 +101,11 @@ def test_skip_flag_makes_the_step_a_no_op(psa, mode):
     flag = torch.zeros(1, dtype=torch.int32, device=DEV)
     psa.adam_step(mode, params, _dev(_grads(1, False)), state, 1, skip_flag=flag)  # flag 0: a real step
     torch.cuda.synchronize()
-    before = [p.cpu().numpy() for p in params] + [s.cpu().numpy() for part in state for s in part]
+    before = [_host(p) for p in params] + [_host(s) for part in state for s in part]
     flag.fill_(1)
     psa.adam_step(mode, params, _dev(_grads(2, False)), state, 2, skip_flag=flag, zero_grads=True)
     torch.cuda.synchronize()
-    after = [p.cpu().numpy() for p in params] + [s.cpu().numpy() for part in state for s in part]
+    after = [_host(p) for p in params] + [_host(s) for part in state for s in part]
     for a, b in zip(before, after):
         np.testing.assert_array_equal(a, b)
 
