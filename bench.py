@@ -172,6 +172,8 @@ def run_ours(args, rank: int, world: int, dist):
     for s in range(n_sets):
         grads.append(workloads.grads_torch(sizes, s + 1, w.grad_std, dev, seed=workloads.DEFAULT_SEED + 1000 * rank,
                                            kind=w.grad_kind, dtype=w.grad_dtype))
+    # with in-step grad zeroing, every step gets its grad set back (outside the step events)
+    pristine = [[g.clone() for g in gs] for gs in grads] if args.zero_grads else None
     try:
         uuid = str(torch.cuda.get_device_properties(dev).uuid)
     except Exception:
@@ -194,6 +196,9 @@ def run_ours(args, rank: int, world: int, dist):
         t = 0
         for _ in range(args.warmup):
             t += 1
+            if pristine is not None:
+                for d, src in zip(grads[(t - 1) % n_sets], pristine[(t - 1) % n_sets]):
+                    d.copy_(src)
             plans[(t - 1) % n_sets].step(t)
         torch.cuda.synchronize(dev)
         if dist is not None:
@@ -202,6 +207,9 @@ def run_ours(args, rank: int, world: int, dist):
         evs = []
         for _ in range(args.steps):
             t += 1
+            if pristine is not None:
+                for d, src in zip(grads[(t - 1) % n_sets], pristine[(t - 1) % n_sets]):
+                    d.copy_(src)
             flush.fill_(float(t))
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)

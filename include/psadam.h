@@ -92,6 +92,10 @@ typedef struct {
     uint64_t seed;               /* Philox key (stochastic rounding only) */
     float percentile;            /* (0, 100]; 100 = absmax. The block's rank k must be <= 16
                                     (percentile >= ~99.27 for full blocks), else UNSUPPORTED */
+    int32_t static_scales;       /* 0: scales recomputed every step (PR #814's default
+                                    UseDynamicQuantization = true). 1: a block keeps its scale
+                                    once it is nonzero (set by its first quantization); values
+                                    beyond it saturate. Steps only; quantize-only ignores it. */
 } psadam_q8_opts;
 
 /* The parameter/gradient side of a multi-tensor list, with the grad-side work that sits on

@@ -43,7 +43,7 @@ class _Scalars(ctypes.Structure):
 
 class _Q8(ctypes.Structure):
     _fields_ = [("stochastic_rounding", ctypes.c_int), ("seed", ctypes.c_uint64),
-                ("percentile", ctypes.c_float)]
+                ("percentile", ctypes.c_float), ("static_scales", ctypes.c_int)]
 
 
 @dataclass(frozen=True)
@@ -63,9 +63,10 @@ class Q8Opts:
     stochastic_rounding: bool = False
     seed: int = 42
     percentile: float = 100.0
+    static_scales: bool = False
 
     def _c(self) -> _Q8:
-        return _Q8(int(self.stochastic_rounding), self.seed, self.percentile)
+        return _Q8(int(self.stochastic_rounding), self.seed, self.percentile, int(self.static_scales))
 
 
 def _load() -> ctypes.CDLL:
@@ -83,7 +84,7 @@ def _load() -> ctypes.CDLL:
         "orc_make_scalars": (_Scalars, [hp, i64]),
         "orc_percentile_rank": (i64, [ctypes.c_float, i64]),
         "orc_kth_largest_abs": (ctypes.c_float, [_f32p, i64, i64]),
-        "orc_quantize_block": (ctypes.c_float, [_f32p, i64, i32, q8, i64, i32, i64, _i8p, _u8p]),
+        "orc_quantize_block": (ctypes.c_float, [_f32p, i64, i32, q8, i64, i32, i64, ctypes.c_float, _i8p, _u8p]),
         "orc_quantize": (None, [i64, _f32p, _f32p, q8, i64, i32, _i8p, _u8p, _f32p, _f32p]),
         "orc_dequantize": (None, [i64, _i8p, _u8p, _f32p, _f32p, _f32p, _f32p]),
         "orc_step_fp32": (None, [i64, _f32p, vp, i32, _f32p, _f32p, hp, i64]),
@@ -168,15 +169,16 @@ def kth_largest_abs(x: np.ndarray, k: int) -> np.float32:
 
 
 def quantize_block(x: np.ndarray, signed: bool, q8: Q8Opts = Q8Opts(), step: int = 1,
-                   tensor_idx: int = 0, elem0: int = 0):
-    """Quantize one block (<= 2048 values). Returns (codes, scale)."""
+                   tensor_idx: int = 0, elem0: int = 0, old_scale: float = 0.0):
+    """Quantize one block (<= 2048 values). Returns (codes, scale). ``old_scale`` is kept
+    when ``q8.static_scales`` and it is nonzero."""
     x = np.ascontiguousarray(x, dtype=np.float32)
     assert x.size <= BLOCK
     codes = np.zeros(x.size, dtype=np.int8 if signed else np.uint8)
     i8 = _ptr(codes, ctypes.c_int8) if signed else None
     u8 = None if signed else _ptr(codes, ctypes.c_uint8)
     s = _lib.orc_quantize_block(_ptr(x, ctypes.c_float), x.size, int(signed), ctypes.byref(q8._c()),
-                                step, tensor_idx, elem0, i8, u8)
+                                step, tensor_idx, elem0, old_scale, i8, u8)
     return codes, np.float32(s)
 
 

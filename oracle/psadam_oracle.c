@@ -226,17 +226,24 @@ float orc_kth_largest_abs(const float* x, int64_t n, int64_t k) {
 }
 
 float orc_quantize_block(const float* x, int64_t n, int is_signed, const orc_q8opts* q,
-                         int64_t step, int tensor_idx, int64_t elem0,
+                         int64_t step, int tensor_idx, int64_t elem0, float old_scale,
                          int8_t* codes_i8, uint8_t* codes_u8) {
-    float absmax = 0.0f;
-    for (int64_t i = 0; i < n; ++i)
-        if (fabsf(x[i]) > absmax) absmax = fabsf(x[i]);
-    int64_t k = orc_percentile_rank(q->percentile, n);
-    float basis = orc_kth_largest_abs(x, n, k);
-    if (basis == 0.0f) basis = absmax; /* a block whose percentile is 0 falls back to its max */
     float qmax = is_signed ? 127.0f : 255.0f;
     float qmin = is_signed ? -127.0f : 0.0f;
-    float scale = basis / qmax;
+    float scale;
+    if (q->static_scales && old_scale != 0.0f) {
+        /* [P814] options list: UseDynamicQuantization = false. Reading: the scale set by
+         * the block's first quantization stays; values beyond it saturate. */
+        scale = old_scale;
+    } else {
+        float absmax = 0.0f;
+        for (int64_t i = 0; i < n; ++i)
+            if (fabsf(x[i]) > absmax) absmax = fabsf(x[i]);
+        int64_t k = orc_percentile_rank(q->percentile, n);
+        float basis = orc_kth_largest_abs(x, n, k);
+        if (basis == 0.0f) basis = absmax; /* a block whose percentile is 0 falls back to its max */
+        scale = basis / qmax;
+    }
     for (int64_t i = 0; i < n; ++i) {
         float r = 0.0f;
         if (scale != 0.0f) {
@@ -266,8 +273,8 @@ void orc_quantize(int64_t n, const float* m, const float* v, const orc_q8opts* q
     for (int64_t b = 0; b < block_count(n); ++b) {
         int64_t lo = b * ORC_BLOCK;
         int64_t cnt = n - lo < ORC_BLOCK ? n - lo : ORC_BLOCK;
-        m_scale[b] = orc_quantize_block(m + lo, cnt, 1, q, step, tensor_idx, lo, m_code + lo, NULL);
-        v_scale[b] = orc_quantize_block(v + lo, cnt, 0, q, step, tensor_idx, lo, NULL, v_code + lo);
+        m_scale[b] = orc_quantize_block(m + lo, cnt, 1, q, step, tensor_idx, lo, m_scale[b], m_code + lo, NULL);
+        v_scale[b] = orc_quantize_block(v + lo, cnt, 0, q, step, tensor_idx, lo, v_scale[b], NULL, v_code + lo);
     }
 }
 
@@ -294,8 +301,8 @@ void orc_step_q8_block(int64_t cnt, int64_t elem0, float* p, const void* grad, i
     for (int64_t i = 0; i < cnt; ++i) mf[i] = (float)m_code[i] * *m_scale;
     for (int64_t i = 0; i < cnt; ++i) vf[i] = (float)v_code[i] * *v_scale;
     for (int64_t i = 0; i < cnt; ++i) adam_element(&p[i], load_grad(grad, grad_bf16, i), &mf[i], &vf[i], &s);
-    *m_scale = orc_quantize_block(mf, cnt, 1, q, t, tensor_idx, elem0, m_code, NULL);
-    *v_scale = orc_quantize_block(vf, cnt, 0, q, t, tensor_idx, elem0, NULL, v_code);
+    *m_scale = orc_quantize_block(mf, cnt, 1, q, t, tensor_idx, elem0, *m_scale, m_code, NULL);
+    *v_scale = orc_quantize_block(vf, cnt, 0, q, t, tensor_idx, elem0, *v_scale, NULL, v_code);
 }
 
 void orc_step_q8(int64_t n, float* p, const void* grad, int grad_bf16, int8_t* m_code,
@@ -321,7 +328,7 @@ void orc_step_q8v_block(int64_t cnt, int64_t elem0, float* p, const void* grad, 
     float vf[ORC_BLOCK];
     for (int64_t i = 0; i < cnt; ++i) vf[i] = (float)v_code[i] * *v_scale;
     for (int64_t i = 0; i < cnt; ++i) adam_element(&p[i], load_grad(grad, grad_bf16, i), &m[i], &vf[i], &s);
-    *v_scale = orc_quantize_block(vf, cnt, 0, q, t, tensor_idx, elem0, NULL, v_code);
+    *v_scale = orc_quantize_block(vf, cnt, 0, q, t, tensor_idx, elem0, *v_scale, NULL, v_code);
 }
 
 void orc_step_q8v(int64_t n, float* p, const void* grad, int grad_bf16, float* m, uint8_t* v_code,

@@ -43,6 +43,7 @@ typedef struct {
     int stochastic_rounding; /* 0 = round to nearest even, 1 = stochastic */
     uint64_t seed;           /* Philox key for stochastic rounding */
     float percentile;        /* scale basis percentile, (0, 100]; 100 = absmax */
+    int static_scales;       /* 1: a block's nonzero scale is kept (frozen) instead of recomputed */
 } orc_q8opts;
 
 /* Philox4x32-10 bijection of one 128-bit counter under a 64-bit key. */
@@ -70,9 +71,11 @@ float orc_kth_largest_abs(const float* x, int64_t n, int64_t k);
 
 /* Quantize one block of n <= ORC_BLOCK values. is_signed: codes in [-127,127]
  * (written to codes_i8), else [0,255] (codes_u8). Returns the block's scale.
- * The stochastic variant draws element (elem0 + i)'s uniform from the step's stream. */
+ * The stochastic variant draws element (elem0 + i)'s uniform from the step's stream.
+ * With q->static_scales and a nonzero old_scale, that scale is kept (no new block
+ * statistics); otherwise old_scale is ignored. */
 float orc_quantize_block(const float* x, int64_t n, int is_signed, const orc_q8opts* q,
-                         int64_t step, int tensor_idx, int64_t elem0,
+                         int64_t step, int tensor_idx, int64_t elem0, float old_scale,
                          int8_t* codes_i8, uint8_t* codes_u8);
 
 /* Whole-tensor quantize / dequantize of a moment pair (block after block). */

@@ -44,7 +44,7 @@ class _HParams(ctypes.Structure):
 
 class _Q8Opts(ctypes.Structure):
     _fields_ = [("block_size", ctypes.c_int32), ("stochastic_rounding", ctypes.c_int32),
-                ("seed", ctypes.c_uint64), ("percentile", ctypes.c_float)]
+                ("seed", ctypes.c_uint64), ("percentile", ctypes.c_float), ("static_scales", ctypes.c_int32)]
 
 
 class _List(ctypes.Structure):
@@ -205,14 +205,15 @@ def adam_step_bf16m(params, grads, m, v, step: int, lr: float = 1e-3, beta1: flo
     _raise(st, "adam_step_bf16m")
 
 
-def _q8(stochastic_rounding: bool, seed: int, percentile: float, block_size: int) -> _Q8Opts:
-    return _Q8Opts(block_size, int(bool(stochastic_rounding)), seed, percentile)
+def _q8(stochastic_rounding: bool, seed: int, percentile: float, block_size: int,
+        static_scales: bool = False) -> _Q8Opts:
+    return _Q8Opts(block_size, int(bool(stochastic_rounding)), seed, percentile, int(bool(static_scales)))
 
 
 def adam_step_q8(params, grads, m_code, v_code, m_scale, v_scale, step: int, lr: float = 1e-3, beta1: float = 0.9,
                  beta2: float = 0.999, eps: float = 1e-8, weight_decay: float = 0.0, stochastic_rounding: bool = False,
                  seed: int = 42, percentile: float = 100.0, block_size: int = BLOCK, grad_unscale: float = 1.0,
-                 zero_grads: bool = False, skip_flag=None, stream=None) -> None:
+                 zero_grads: bool = False, skip_flag=None, static_scales: bool = False, stream=None) -> None:
     """One AdamW step with 8-bit block-wise moments (int8 m codes, uint8 v codes, fp32
     per-block scales), dequantize-update-requantize in one pass, in place."""
     lst, keep = _list(params, grads, grad_unscale, zero_grads, skip_flag)
@@ -223,7 +224,7 @@ def adam_step_q8(params, grads, m_code, v_code, m_scale, v_scale, step: int, lr:
     ptrs = [_ptrs(x) for x in (m_code, v_code, m_scale, v_scale)]
     st = _lib.adam_step_q8(ctypes.byref(lst), *[ctypes.cast(p, _PP) for p in ptrs], step,
                            ctypes.byref(_hp(lr, beta1, beta2, eps, weight_decay)),
-                           ctypes.byref(_q8(stochastic_rounding, seed, percentile, block_size)),
+                           ctypes.byref(_q8(stochastic_rounding, seed, percentile, block_size, static_scales)),
                            _stream_handle(stream, params))
     _raise(st, "adam_step_q8")
 
@@ -231,7 +232,7 @@ def adam_step_q8(params, grads, m_code, v_code, m_scale, v_scale, step: int, lr:
 def adam_step_q8v(params, grads, m, v_code, v_scale, step: int, lr: float = 1e-3, beta1: float = 0.9,
                   beta2: float = 0.999, eps: float = 1e-8, weight_decay: float = 0.0, stochastic_rounding: bool = False,
                   seed: int = 42, percentile: float = 100.0, block_size: int = BLOCK, grad_unscale: float = 1.0,
-                  zero_grads: bool = False, skip_flag=None, stream=None) -> None:
+                  zero_grads: bool = False, skip_flag=None, static_scales: bool = False, stream=None) -> None:
     """One AdamW step with an fp32 first moment and an 8-bit block-wise second moment
     (uint8 v codes, fp32 per-block scales), in place."""
     lst, keep = _list(params, grads, grad_unscale, zero_grads, skip_flag)
@@ -241,7 +242,7 @@ def adam_step_q8v(params, grads, m, v_code, v_scale, step: int, lr: float = 1e-3
     ptrs = [_ptrs(x) for x in (m, v_code, v_scale)]
     st = _lib.adam_step_q8v(ctypes.byref(lst), *[ctypes.cast(p, _PP) for p in ptrs], step,
                             ctypes.byref(_hp(lr, beta1, beta2, eps, weight_decay)),
-                            ctypes.byref(_q8(stochastic_rounding, seed, percentile, block_size)),
+                            ctypes.byref(_q8(stochastic_rounding, seed, percentile, block_size, static_scales)),
                             _stream_handle(stream, params))
     _raise(st, "adam_step_q8v")
 
@@ -334,7 +335,8 @@ class StepPlan:
     def __init__(self, mode: str, params, grads, state, lr: float = 1e-3, beta1: float = 0.9,
                  beta2: float = 0.999, eps: float = 1e-8, weight_decay: float = 0.0,
                  stochastic_rounding: bool = False, seed: int = 42, percentile: float = 100.0,
-                 block_size: int = BLOCK, grad_unscale: float = 1.0, zero_grads: bool = False, skip_flag=None):
+                 block_size: int = BLOCK, grad_unscale: float = 1.0, zero_grads: bool = False, skip_flag=None,
+                 static_scales: bool = False):
         if mode not in MODES:
             raise ValueError(f"unknown moment mode {mode!r}")
         self.mode = mode
@@ -361,7 +363,7 @@ class StepPlan:
         self._state_pp = [ctypes.cast(p, _PP) for p in self._state_ptrs]
         self._state = state
         self._hp = _hp(lr, beta1, beta2, eps, weight_decay)
-        self._q8 = _q8(stochastic_rounding, seed, percentile, block_size)
+        self._q8 = _q8(stochastic_rounding, seed, percentile, block_size, static_scales)
 
     def set_grads(self, grads) -> None:
         if len(grads) != len(self._params):

@@ -48,6 +48,7 @@ int check_q8(const psadam_q8_opts* q) {
   if (q->block_size != kBlock) return PSADAM_ERR_UNSUPPORTED;
   if (q->stochastic_rounding != 0 && q->stochastic_rounding != 1) return PSADAM_ERR_INVALID_ARG;
   if (!finite(q->percentile) || !(q->percentile > 0.f) || q->percentile > 100.f) return PSADAM_ERR_INVALID_ARG;
+  if (q->static_scales != 0 && q->static_scales != 1) return PSADAM_ERR_INVALID_ARG;
   return PSADAM_OK;
 }
 
@@ -112,6 +113,7 @@ struct GradSide {
   float unscale = 1.0f;
   int zero = 0;
   const int* skip = nullptr;
+  int static_scales = 0;  // not grad-side, but carried the same way into the launch
 };
 
 // Pack the list into as few launches as fit and run `fn` on each.
@@ -124,6 +126,7 @@ int run_launches(const std::vector<Entry>& es, const StepConsts& c, uint64_t see
   a.g_unscale = gs.unscale;
   a.zero_grads = gs.zero;
   a.skip = gs.skip;
+  a.static_scales = gs.static_scales;
   a.seed_lo = (uint32_t)(seed & 0xFFFFFFFFu);
   a.seed_hi = (uint32_t)(seed >> 32);
   a.step_lo = (uint32_t)step;
@@ -249,6 +252,7 @@ int step_common(int mode, const psadam_list* list, const void* const* m, const v
   if (kmax > kMaxRank) return PSADAM_ERR_UNSUPPORTED;
   GradSide gs;
   if ((st = grad_side(list, gs)) != PSADAM_OK) return st;
+  gs.static_scales = q8mode && q8->static_scales != 0;
   const int K = rank_template(kmax);
   const bool gb = list->grad_dtype == PSADAM_GRAD_BF16;
   const StepConsts c = make_consts(*hp, step);

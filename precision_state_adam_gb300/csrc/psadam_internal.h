@@ -53,6 +53,8 @@ struct LaunchArgs {
   float g_unscale;  // grads are multiplied by this before use (1: unchanged)
   int zero_grads;   // nonzero: overwrite each grad with zero after reading it
   const int* skip;  // device flag or null: a nonzero value makes the launch a no-op
+  int static_scales;  // 8-bit: a block's nonzero scale is kept instead of recomputed
+  int pad_;
   TensorRef t[CAP];
 };
 static_assert(sizeof(LaunchArgs<kCapLarge>) <= 32764, "kernel parameter block too large");

@@ -119,5 +119,8 @@ def hp_kwargs(hp: HParams) -> dict:
     return dict(lr=hp.lr, beta1=hp.beta1, beta2=hp.beta2, eps=hp.eps, weight_decay=hp.weight_decay)
 
 
-def q8_kwargs(q8: Q8Opts) -> dict:
-    return dict(stochastic_rounding=q8.stochastic_rounding, seed=q8.seed, percentile=q8.percentile)
+def q8_kwargs(q8: Q8Opts, step: bool = True) -> dict:
+    kw = dict(stochastic_rounding=q8.stochastic_rounding, seed=q8.seed, percentile=q8.percentile)
+    if step:
+        kw["static_scales"] = q8.static_scales
+    return kw

@@ -106,6 +106,8 @@ Q8_CASES = {
     "rne_p99.9": Q8Opts(False, 42, 99.9),   # rank 3 of a full block (K = 4 kernel)
     "sr_p99.9": Q8Opts(True, 7, 99.9),
     "rne_p99.5": Q8Opts(False, 42, 99.5),   # rank 11 (K = 16 kernel)
+    "rne_static": Q8Opts(False, 42, 100.0, True),  # scales kept after the first step
+    "sr_static_p99.9": Q8Opts(True, 5, 99.9, True),
 }
 
 
@@ -163,7 +165,7 @@ def test_quantize_only_is_bit_exact(psa, case):
         vs.append(v)
     dm, dv = _to_dev(ms), _to_dev(vs)
     mc, vc, msc, vsc = psa.zeros_state(dm, "q8")
-    psa.q8_quantize(dm, dv, mc, vc, msc, vsc, step=9, **q8_kwargs(q8))
+    psa.q8_quantize(dm, dv, mc, vc, msc, vsc, step=9, **q8_kwargs(q8, step=False))
     torch.cuda.synchronize()
     for i, n in enumerate(sizes):
         want = oracle.quantize(ms[i], vs[i], q8, step=9, tensor_idx=i)

@@ -527,3 +527,38 @@ def test_grad_unscale_is_one_rounding_of_the_product():
     np.testing.assert_array_equal(oracle.unscale_grads(gb, u), (wide.astype(np.float64) * u).astype(F32))
     # overflow of the product is an inf the check must catch
     assert np.isinf(oracle.unscale_grads(np.array([3e38], F32), 10.0)[0])
+
+
+def test_static_scales_freeze_after_the_first_quantization():
+    """UseDynamicQuantization = false (PR #814 options): the first step sets each block's
+    scale as the dynamic mode would; later steps keep it, and codes are the nearest code
+    under the kept scale, saturating."""
+    hp = HParams(lr=1e-3, weight_decay=0.0)
+    n = 2048 * 2 + 77
+    p, g1 = _fresh(n, seed=51, std=1e-3)
+    nb = oracle.n_blocks(n)
+    q_dyn, q_sta = Q8Opts(), Q8Opts(static_scales=True)
+    sd = [p.copy(), np.zeros(n, np.int8), np.zeros(n, np.uint8), np.zeros(nb, F32), np.zeros(nb, F32)]
+    ss = [x.copy() for x in sd]
+    oracle.step_q8(*sd[:1], g1, *sd[1:], 1, hp, q_dyn)
+    oracle.step_q8(*ss[:1], g1, *ss[1:], 1, hp, q_sta)
+    for a, b in zip(sd, ss):
+        np.testing.assert_array_equal(a, b)
+    # step 2 with grads 4x larger: the kept scales saturate some codes
+    _, g2 = _fresh(n, seed=52, std=4e-3)
+    m1, v1 = oracle.dequantize(*ss[1:])
+    pf, mf, vf = ss[0].copy(), m1.copy(), v1.copy()
+    oracle.step_fp32(pf, g2, mf, vf, 2, hp)
+    s_m, s_v = ss[3].copy(), ss[4].copy()
+    oracle.step_q8(*ss[:1], g2, *ss[1:], 2, hp, q_sta)
+    np.testing.assert_array_equal(ss[3], s_m)
+    np.testing.assert_array_equal(ss[4], s_v)
+    np.testing.assert_array_equal(ss[0], pf)
+    blk = np.arange(n) // 2048
+    for x, codes, s, lo, hi in ((mf, ss[1], s_m, -127, 127), (vf, ss[2], s_v, 0, 255)):
+        ratio = x.astype(np.float64) / s[blk].astype(np.float64)
+        want = np.clip(np.rint(ratio), lo, hi)
+        near_half = np.abs(ratio - np.floor(ratio) - 0.5) < 2.0 ** -16
+        got = codes.astype(np.float64)
+        assert np.all((got == want) | near_half)
+    assert np.any(np.abs(ss[1].astype(int)) == 127) and np.mean(np.abs(ss[1].astype(int)) == 127) > 0.01
