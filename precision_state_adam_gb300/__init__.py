@@ -391,3 +391,6 @@ class StepPlan:
 def cdll() -> ctypes.CDLL:
     """The loaded libpsadam.so handle (for ABI-level tests)."""
     return _lib
+
+
+from .serialize import StateFormatError, load_state, save_state  # noqa: E402  (host-side state files)

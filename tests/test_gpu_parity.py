@@ -254,6 +254,41 @@ def test_resume_equals_uninterrupted(psa):
             np.testing.assert_array_equal(a, b)
 
 
+@pytest.mark.parametrize("mode", ["fp32", "bf16m", "q8", "q8v"])
+def test_resume_through_state_file(psa, mode, tmp_path):
+    """k steps, state written with save_state and read back with load_state, then N-k
+    steps == N straight steps, bit for bit, for every moment mode."""
+    sizes = [5000, 0, 2048 * 3 + 5]
+    hp = HParams(weight_decay=0.01)
+    q8 = Q8Opts(True, 7, 99.9)
+    specs = [workloads.TensorSpec(f"t{i}", (n,)) for i, n in enumerate(sizes)]
+    p0 = workloads.init_params_np(specs, seed=4)
+    step_fn = {"fp32": psa.adam_step_fp32, "bf16m": psa.adam_step_bf16m,
+               "q8": psa.adam_step_q8, "q8v": psa.adam_step_q8v}[mode]
+    extra = q8_kwargs(q8) if mode in ("q8", "q8v") else {}
+    path = str(tmp_path / "state.bin")
+    runs = []
+    for split in (None, 2):
+        params = _to_dev(p0)
+        state = psa.zeros_state(params, mode)
+        for t in range(1, 6):
+            if split is not None and t == split + 1:
+                psa.save_state(path, mode, state, t - 1, hparams=hp_kwargs(hp))
+                del state
+                mode2, state, last, _ = psa.load_state(path, device=DEV)
+                assert mode2 == mode and last == t - 1
+            grads = _to_dev(workloads.grads_np(sizes, t, 1e-3, seed=4))
+            step_fn(params, grads, *state, t, **hp_kwargs(hp), **extra)
+        runs.append(([p.cpu().numpy() for p in params],
+                     [[(s.view(torch.int16) if s.dtype == torch.bfloat16 else s).cpu().numpy() for s in part]
+                      for part in state]))
+    for a, b in zip(runs[0][0], runs[1][0]):
+        np.testing.assert_array_equal(a, b)
+    for pa, pb in zip(runs[0][1], runs[1][1]):
+        for a, b in zip(pa, pb):
+            np.testing.assert_array_equal(a, b)
+
+
 def test_runs_on_the_callers_stream(psa):
     n = 300000
     p0 = workloads.init_params_np([workloads.TensorSpec("w", (n,))], seed=6)[0]

@@ -1,0 +1,68 @@
+"""State files (host side): round trip for every moment mode, the pages' flags (both
+moments compressed / a quantized v follows), and rejection of damaged or mismatched files."""
+import io
+import os
+
+import pytest
+import torch
+
+
+@pytest.fixture(scope="module")
+def psa():
+    import __graft_entry__
+    __graft_entry__.build()
+    import precision_state_adam_gb300 as psa
+    return psa
+
+
+def _random_state(mode, sizes, seed=0):
+    g = torch.Generator().manual_seed(seed)
+    nb = lambda n: (n + 2047) // 2048
+    if mode == "fp32":
+        return ([torch.randn(n, generator=g) for n in sizes], [torch.rand(n, generator=g) for n in sizes])
+    if mode == "bf16m":
+        return ([torch.randn(n, generator=g).bfloat16() for n in sizes],
+                [torch.rand(n, generator=g).bfloat16() for n in sizes])
+    if mode == "q8":
+        return ([torch.randint(-127, 128, (n,), generator=g, dtype=torch.int8) for n in sizes],
+                [torch.randint(0, 256, (n,), generator=g, dtype=torch.uint8) for n in sizes],
+                [torch.rand(nb(n), generator=g) for n in sizes], [torch.rand(nb(n), generator=g) for n in sizes])
+    return ([torch.randn(n, generator=g) for n in sizes],
+            [torch.randint(0, 256, (n,), generator=g, dtype=torch.uint8) for n in sizes],
+            [torch.rand(nb(n), generator=g) for n in sizes])
+
+
+@pytest.mark.parametrize("mode", ["fp32", "bf16m", "q8", "q8v"])
+def test_round_trip_is_bit_exact(psa, mode, tmp_path):
+    sizes = [1, 2047, 2049, 5000, 0]
+    st = _random_state(mode, sizes)
+    path = os.path.join(tmp_path, "state.bin")
+    psa.save_state(path, mode, st, step=17, hparams={"lr": 1e-3}, q8={"percentile": 99.9})
+    mode2, st2, step, header = psa.load_state(path)
+    assert mode2 == mode and step == 17 and header["hparams"]["lr"] == 1e-3
+    assert header["compress_both_moments"] == (mode == "q8")
+    assert header["has_v_quantized"] == (mode in ("q8", "q8v"))
+    for a_part, b_part in zip(st, st2):
+        for a, b in zip(a_part, b_part):
+            assert a.dtype == b.dtype and a.shape == b.shape
+            if a.dtype == torch.bfloat16:
+                a, b = a.view(torch.int16), b.view(torch.int16)
+            assert torch.equal(a, b)
+
+
+def test_damaged_and_mismatched_files_are_rejected(psa):
+    st = _random_state("q8", [3000])
+    buf = io.BytesIO()
+    psa.save_state(buf, "q8", st, step=2)
+    data = bytearray(buf.getvalue())
+    flipped = bytearray(data)
+    flipped[len(flipped) // 2] ^= 0x40
+    with pytest.raises(psa.StateFormatError, match="checksum"):
+        psa.load_state(io.BytesIO(bytes(flipped)))
+    with pytest.raises(psa.StateFormatError, match="not a psadam"):
+        psa.load_state(io.BytesIO(b"XXXXXXXX" + bytes(data[8:])))
+    with pytest.raises(ValueError):
+        psa.save_state(io.BytesIO(), "q8", st[:3], step=1)  # a part is missing
+    with pytest.raises(ValueError):
+        bad = (st[0], st[1], st[2], [torch.zeros(5)])  # wrong scale count
+        psa.save_state(io.BytesIO(), "q8", bad, step=1)
