@@ -43,7 +43,7 @@ class _Scalars(ctypes.Structure):
 
 class _Q8(ctypes.Structure):
     _fields_ = [("stochastic_rounding", ctypes.c_int), ("seed", ctypes.c_uint64),
-                ("percentile", ctypes.c_float), ("static_scales", ctypes.c_int)]
+                ("percentile", ctypes.c_float), ("static_scales", ctypes.c_int), ("block_size", ctypes.c_int)]
 
 
 @dataclass(frozen=True)
@@ -64,9 +64,12 @@ class Q8Opts:
     seed: int = 42
     percentile: float = 100.0
     static_scales: bool = False
+    block_size: int = BLOCK
 
     def _c(self) -> _Q8:
-        return _Q8(int(self.stochastic_rounding), self.seed, self.percentile, int(self.static_scales))
+        assert self.block_size >= 1, "block size must be positive"
+        return _Q8(int(self.stochastic_rounding), self.seed, self.percentile, int(self.static_scales),
+                   self.block_size)
 
 
 def _load() -> ctypes.CDLL:
@@ -86,7 +89,7 @@ def _load() -> ctypes.CDLL:
         "orc_kth_largest_abs": (ctypes.c_float, [_f32p, i64, i64]),
         "orc_quantize_block": (ctypes.c_float, [_f32p, i64, i32, q8, i64, i32, i64, ctypes.c_float, _i8p, _u8p]),
         "orc_quantize": (None, [i64, _f32p, _f32p, q8, i64, i32, _i8p, _u8p, _f32p, _f32p]),
-        "orc_dequantize": (None, [i64, _i8p, _u8p, _f32p, _f32p, _f32p, _f32p]),
+        "orc_dequantize": (None, [i64, i64, _i8p, _u8p, _f32p, _f32p, _f32p, _f32p]),
         "orc_step_fp32": (None, [i64, _f32p, vp, i32, _f32p, _f32p, hp, i64]),
         "orc_step_bf16m": (None, [i64, _f32p, vp, i32, _u16p, _u16p, hp, i64]),
         "orc_step_q8": (None, [i64, _f32p, vp, i32, _i8p, _u8p, _f32p, _f32p, hp, i64, q8, i32,
@@ -119,8 +122,8 @@ def _check(a: np.ndarray, dtype, name: str, n: int | None = None) -> None:
         raise ValueError(f"{name}: expected {n} elements, got {a.size}")
 
 
-def n_blocks(n: int) -> int:
-    return (n + BLOCK - 1) // BLOCK
+def n_blocks(n: int, block_size: int = BLOCK) -> int:
+    return (n + block_size - 1) // block_size
 
 
 # ---------------------------------------------------------------- primitives
@@ -170,10 +173,9 @@ def kth_largest_abs(x: np.ndarray, k: int) -> np.float32:
 
 def quantize_block(x: np.ndarray, signed: bool, q8: Q8Opts = Q8Opts(), step: int = 1,
                    tensor_idx: int = 0, elem0: int = 0, old_scale: float = 0.0):
-    """Quantize one block (<= 2048 values). Returns (codes, scale). ``old_scale`` is kept
-    when ``q8.static_scales`` and it is nonzero."""
+    """Quantize one block of ``x.size`` values. Returns (codes, scale). ``old_scale`` is
+    kept when ``q8.static_scales`` and it is nonzero."""
     x = np.ascontiguousarray(x, dtype=np.float32)
-    assert x.size <= BLOCK
     codes = np.zeros(x.size, dtype=np.int8 if signed else np.uint8)
     i8 = _ptr(codes, ctypes.c_int8) if signed else None
     u8 = None if signed else _ptr(codes, ctypes.c_uint8)
@@ -189,23 +191,23 @@ def quantize(m: np.ndarray, v: np.ndarray, q8: Q8Opts = Q8Opts(), step: int = 1,
     _check(v, np.float32, "v", n)
     mc = np.zeros(n, np.int8)
     vc = np.zeros(n, np.uint8)
-    ms = np.zeros(n_blocks(n), np.float32)
-    vs = np.zeros(n_blocks(n), np.float32)
+    ms = np.zeros(n_blocks(n, q8.block_size), np.float32)
+    vs = np.zeros(n_blocks(n, q8.block_size), np.float32)
     _lib.orc_quantize(n, _ptr(m, ctypes.c_float), _ptr(v, ctypes.c_float), ctypes.byref(q8._c()), step,
                       tensor_idx, _ptr(mc, ctypes.c_int8), _ptr(vc, ctypes.c_uint8),
                       _ptr(ms, ctypes.c_float), _ptr(vs, ctypes.c_float))
     return mc, vc, ms, vs
 
 
-def dequantize(mc, vc, ms, vs):
+def dequantize(mc, vc, ms, vs, block_size: int = BLOCK):
     n = mc.size
     _check(mc, np.int8, "m_code")
     _check(vc, np.uint8, "v_code", n)
-    _check(ms, np.float32, "m_scale", n_blocks(n))
-    _check(vs, np.float32, "v_scale", n_blocks(n))
+    _check(ms, np.float32, "m_scale", n_blocks(n, block_size))
+    _check(vs, np.float32, "v_scale", n_blocks(n, block_size))
     m = np.empty(n, np.float32)
     v = np.empty(n, np.float32)
-    _lib.orc_dequantize(n, _ptr(mc, ctypes.c_int8), _ptr(vc, ctypes.c_uint8), _ptr(ms, ctypes.c_float),
+    _lib.orc_dequantize(n, block_size, _ptr(mc, ctypes.c_int8), _ptr(vc, ctypes.c_uint8), _ptr(ms, ctypes.c_float),
                         _ptr(vs, ctypes.c_float), _ptr(m, ctypes.c_float), _ptr(v, ctypes.c_float))
     return m, v
 
@@ -247,10 +249,11 @@ def step_q8(p, g, mc, vc, ms, vs, t: int, hp: HParams, q8: Q8Opts = Q8Opts(), te
     _check(p, np.float32, "param")
     _check(mc, np.int8, "m_code", n)
     _check(vc, np.uint8, "v_code", n)
-    _check(ms, np.float32, "m_scale", n_blocks(n))
-    _check(vs, np.float32, "v_scale", n_blocks(n))
-    b0, b1 = blocks if blocks is not None else (0, n_blocks(n))
-    assert 0 <= b0 <= b1 <= n_blocks(n)
+    nb = n_blocks(n, q8.block_size)
+    _check(ms, np.float32, "m_scale", nb)
+    _check(vs, np.float32, "v_scale", nb)
+    b0, b1 = blocks if blocks is not None else (0, nb)
+    assert 0 <= b0 <= b1 <= nb
     gp, gb = _grad(g, n)
     _lib.orc_step_q8(n, _ptr(p, ctypes.c_float), gp, gb, _ptr(mc, ctypes.c_int8), _ptr(vc, ctypes.c_uint8),
                      _ptr(ms, ctypes.c_float), _ptr(vs, ctypes.c_float), ctypes.byref(hp._c()), t,
@@ -259,10 +262,10 @@ def step_q8(p, g, mc, vc, ms, vs, t: int, hp: HParams, q8: Q8Opts = Q8Opts(), te
 
 def step_q8_block(p, g, mc, vc, ms, vs, t: int, hp: HParams, q8: Q8Opts, tensor_idx: int, elem0: int) -> None:
     """8-bit step of one block held in its own arrays: ``p, g, mc, vc`` are the block's
-    elements (<= 2048), ``ms, vs`` one-element scale arrays, ``elem0`` the block's first
+    elements (at most ``q8.block_size``), ``ms, vs`` one-element scale arrays, ``elem0`` the block's first
     element index within its tensor (it keys the stochastic-rounding stream)."""
     n = p.size
-    assert 0 < n <= BLOCK and elem0 % BLOCK == 0
+    assert 0 < n <= q8.block_size and elem0 % q8.block_size == 0
     _check(p, np.float32, "param")
     _check(mc, np.int8, "m_code", n)
     _check(vc, np.uint8, "v_code", n)
@@ -281,9 +284,10 @@ def step_q8v(p, g, m, vc, vs, t: int, hp: HParams, q8: Q8Opts = Q8Opts(), tensor
     _check(p, np.float32, "param")
     _check(m, np.float32, "m", n)
     _check(vc, np.uint8, "v_code", n)
-    _check(vs, np.float32, "v_scale", n_blocks(n))
-    b0, b1 = blocks if blocks is not None else (0, n_blocks(n))
-    assert 0 <= b0 <= b1 <= n_blocks(n)
+    nb = n_blocks(n, q8.block_size)
+    _check(vs, np.float32, "v_scale", nb)
+    b0, b1 = blocks if blocks is not None else (0, nb)
+    assert 0 <= b0 <= b1 <= nb
     gp, gb = _grad(g, n)
     _lib.orc_step_q8v(n, _ptr(p, ctypes.c_float), gp, gb, _ptr(m, ctypes.c_float), _ptr(vc, ctypes.c_uint8),
                       _ptr(vs, ctypes.c_float), ctypes.byref(hp._c()), t, ctypes.byref(q8._c()), tensor_idx, b0, b1)
@@ -292,7 +296,7 @@ def step_q8v(p, g, m, vc, vs, t: int, hp: HParams, q8: Q8Opts = Q8Opts(), tensor
 def step_q8v_block(p, g, m, vc, vs, t: int, hp: HParams, q8: Q8Opts, tensor_idx: int, elem0: int) -> None:
     """One block of the fp32-m / 8-bit-v step, held in its own arrays (see step_q8_block)."""
     n = p.size
-    assert 0 < n <= BLOCK and elem0 % BLOCK == 0
+    assert 0 < n <= q8.block_size and elem0 % q8.block_size == 0
     _check(p, np.float32, "param")
     _check(m, np.float32, "m", n)
     _check(vc, np.uint8, "v_code", n)

@@ -194,6 +194,7 @@ void orc_step_bf16m(int64_t n, float* p, const void* grad, int grad_bf16, uint16
 
 /* ------------------------------------------------------------------------------ */
 /* Block-wise 8-bit moments — [P814] summary: block-wise quantization, block 2048,  */
+/* (options list: BlockSize, any positive size, default 2048),                     */
 /* signed quantization for m and unsigned for v, dynamic scales, percentile-based  */
 /* scaling (QuantizationPercentile, default 99.9, range 0..100), optional          */
 /* stochastic rounding; review notes: "[-127, 127] to [1, 255] mapping (0 is       */
@@ -265,24 +266,25 @@ float orc_quantize_block(const float* x, int64_t n, int is_signed, const orc_q8o
     return scale;
 }
 
-static int64_t block_count(int64_t n) { return (n + ORC_BLOCK - 1) / ORC_BLOCK; }
+static int64_t block_count(int64_t n, int64_t bs) { return (n + bs - 1) / bs; }
 
 void orc_quantize(int64_t n, const float* m, const float* v, const orc_q8opts* q,
                   int64_t step, int tensor_idx, int8_t* m_code, uint8_t* v_code,
                   float* m_scale, float* v_scale) {
-    for (int64_t b = 0; b < block_count(n); ++b) {
-        int64_t lo = b * ORC_BLOCK;
-        int64_t cnt = n - lo < ORC_BLOCK ? n - lo : ORC_BLOCK;
+    const int64_t bs = q->block_size;
+    for (int64_t b = 0; b < block_count(n, bs); ++b) {
+        int64_t lo = b * bs;
+        int64_t cnt = n - lo < bs ? n - lo : bs;
         m_scale[b] = orc_quantize_block(m + lo, cnt, 1, q, step, tensor_idx, lo, m_scale[b], m_code + lo, NULL);
         v_scale[b] = orc_quantize_block(v + lo, cnt, 0, q, step, tensor_idx, lo, v_scale[b], NULL, v_code + lo);
     }
 }
 
 /* Dequantize: value = code * scale, one single-precision multiply. */
-void orc_dequantize(int64_t n, const int8_t* m_code, const uint8_t* v_code,
+void orc_dequantize(int64_t n, int64_t block_size, const int8_t* m_code, const uint8_t* v_code,
                     const float* m_scale, const float* v_scale, float* m, float* v) {
     for (int64_t i = 0; i < n; ++i) {
-        int64_t b = i / ORC_BLOCK;
+        int64_t b = i / block_size;
         m[i] = (float)m_code[i] * m_scale[b];
         v[i] = (float)v_code[i] * v_scale[b];
     }
@@ -297,12 +299,15 @@ void orc_step_q8_block(int64_t cnt, int64_t elem0, float* p, const void* grad, i
                        int8_t* m_code, uint8_t* v_code, float* m_scale, float* v_scale,
                        const orc_hparams* hp, int64_t t, const orc_q8opts* q, int tensor_idx) {
     orc_scalars s = orc_make_scalars(hp, t);
-    float mf[ORC_BLOCK], vf[ORC_BLOCK];
+    float* mf = (float*)malloc((size_t)cnt * sizeof(float));
+    float* vf = (float*)malloc((size_t)cnt * sizeof(float));
     for (int64_t i = 0; i < cnt; ++i) mf[i] = (float)m_code[i] * *m_scale;
     for (int64_t i = 0; i < cnt; ++i) vf[i] = (float)v_code[i] * *v_scale;
     for (int64_t i = 0; i < cnt; ++i) adam_element(&p[i], load_grad(grad, grad_bf16, i), &mf[i], &vf[i], &s);
     *m_scale = orc_quantize_block(mf, cnt, 1, q, t, tensor_idx, elem0, *m_scale, m_code, NULL);
     *v_scale = orc_quantize_block(vf, cnt, 0, q, t, tensor_idx, elem0, *v_scale, NULL, v_code);
+    free(mf);
+    free(vf);
 }
 
 void orc_step_q8(int64_t n, float* p, const void* grad, int grad_bf16, int8_t* m_code,
@@ -310,9 +315,10 @@ void orc_step_q8(int64_t n, float* p, const void* grad, int grad_bf16, int8_t* m
                  int64_t t, const orc_q8opts* q, int tensor_idx, int64_t block_begin,
                  int64_t block_end) {
     size_t gsize = grad_bf16 ? sizeof(uint16_t) : sizeof(float);
+    const int64_t bs = q->block_size;
     for (int64_t b = block_begin; b < block_end; ++b) {
-        int64_t lo = b * ORC_BLOCK;
-        int64_t cnt = n - lo < ORC_BLOCK ? n - lo : ORC_BLOCK;
+        int64_t lo = b * bs;
+        int64_t cnt = n - lo < bs ? n - lo : bs;
         orc_step_q8_block(cnt, lo, p + lo, (const char*)grad + (size_t)lo * gsize, grad_bf16,
                           m_code + lo, v_code + lo, m_scale + b, v_scale + b, hp, t, q, tensor_idx);
     }
@@ -325,19 +331,21 @@ void orc_step_q8v_block(int64_t cnt, int64_t elem0, float* p, const void* grad, 
                         uint8_t* v_code, float* v_scale, const orc_hparams* hp, int64_t t,
                         const orc_q8opts* q, int tensor_idx) {
     orc_scalars s = orc_make_scalars(hp, t);
-    float vf[ORC_BLOCK];
+    float* vf = (float*)malloc((size_t)cnt * sizeof(float));
     for (int64_t i = 0; i < cnt; ++i) vf[i] = (float)v_code[i] * *v_scale;
     for (int64_t i = 0; i < cnt; ++i) adam_element(&p[i], load_grad(grad, grad_bf16, i), &m[i], &vf[i], &s);
     *v_scale = orc_quantize_block(vf, cnt, 0, q, t, tensor_idx, elem0, *v_scale, NULL, v_code);
+    free(vf);
 }
 
 void orc_step_q8v(int64_t n, float* p, const void* grad, int grad_bf16, float* m, uint8_t* v_code,
                   float* v_scale, const orc_hparams* hp, int64_t t, const orc_q8opts* q, int tensor_idx,
                   int64_t block_begin, int64_t block_end) {
     size_t gsize = grad_bf16 ? sizeof(uint16_t) : sizeof(float);
+    const int64_t bs = q->block_size;
     for (int64_t b = block_begin; b < block_end; ++b) {
-        int64_t lo = b * ORC_BLOCK;
-        int64_t cnt = n - lo < ORC_BLOCK ? n - lo : ORC_BLOCK;
+        int64_t lo = b * bs;
+        int64_t cnt = n - lo < bs ? n - lo : bs;
         orc_step_q8v_block(cnt, lo, p + lo, (const char*)grad + (size_t)lo * gsize, grad_bf16, m + lo,
                            v_code + lo, v_scale + b, hp, t, q, tensor_idx);
     }

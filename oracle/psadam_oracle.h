@@ -26,7 +26,7 @@
 extern "C" {
 #endif
 
-#define ORC_BLOCK 2048
+#define ORC_BLOCK 2048 /* [P814] default BlockSize */
 
 /* Hyper-parameters exactly as a caller hands them over (single precision). */
 typedef struct {
@@ -44,6 +44,7 @@ typedef struct {
     uint64_t seed;           /* Philox key for stochastic rounding */
     float percentile;        /* scale basis percentile, (0, 100]; 100 = absmax */
     int static_scales;       /* 1: a block's nonzero scale is kept (frozen) instead of recomputed */
+    int block_size;          /* elements per quantization block (>= 1; [P814] default 2048) */
 } orc_q8opts;
 
 /* Philox4x32-10 bijection of one 128-bit counter under a 64-bit key. */
@@ -69,7 +70,7 @@ int64_t orc_percentile_rank(float pct, int64_t n);
 /* k-th largest of |x[0..n)| (k is 1-based, 1 <= k <= n). */
 float orc_kth_largest_abs(const float* x, int64_t n, int64_t k);
 
-/* Quantize one block of n <= ORC_BLOCK values. is_signed: codes in [-127,127]
+/* Quantize one block of n values (n <= the block size). is_signed: codes in [-127,127]
  * (written to codes_i8), else [0,255] (codes_u8). Returns the block's scale.
  * The stochastic variant draws element (elem0 + i)'s uniform from the step's stream.
  * With q->static_scales and a nonzero old_scale, that scale is kept (no new block
@@ -82,7 +83,7 @@ float orc_quantize_block(const float* x, int64_t n, int is_signed, const orc_q8o
 void orc_quantize(int64_t n, const float* m, const float* v, const orc_q8opts* q,
                   int64_t step, int tensor_idx, int8_t* m_code, uint8_t* v_code,
                   float* m_scale, float* v_scale);
-void orc_dequantize(int64_t n, const int8_t* m_code, const uint8_t* v_code,
+void orc_dequantize(int64_t n, int64_t block_size, const int8_t* m_code, const uint8_t* v_code,
                     const float* m_scale, const float* v_scale, float* m, float* v);
 
 /* One AdamW step over one tensor of n elements, in place.
@@ -91,14 +92,14 @@ void orc_step_fp32(int64_t n, float* p, const void* grad, int grad_bf16, float* 
                    const orc_hparams* hp, int64_t t);
 void orc_step_bf16m(int64_t n, float* p, const void* grad, int grad_bf16, uint16_t* m,
                     uint16_t* v, const orc_hparams* hp, int64_t t);
-/* 8-bit moments over blocks [block_begin, block_end) of the tensor; the rest of the
+/* 8-bit moments over blocks [block_begin, block_end) of q->block_size elements; the rest of the
  * tensor is left untouched (steps are block-local, so a range is exact). */
 void orc_step_q8(int64_t n, float* p, const void* grad, int grad_bf16, int8_t* m_code,
                  uint8_t* v_code, float* m_scale, float* v_scale, const orc_hparams* hp,
                  int64_t t, const orc_q8opts* q, int tensor_idx, int64_t block_begin,
                  int64_t block_end);
 
-/* The same step for one block: cnt (<= ORC_BLOCK) valid elements that start at element
+/* The same step for one block: cnt (<= q->block_size) valid elements that start at element
  * elem0 of their tensor; array pointers point at the block's first element and the
  * scale pointers at the block's own scale. */
 void orc_step_q8_block(int64_t cnt, int64_t elem0, float* p, const void* grad, int grad_bf16,

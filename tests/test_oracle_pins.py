@@ -562,3 +562,98 @@ def test_static_scales_freeze_after_the_first_quantization():
         got = codes.astype(np.float64)
         assert np.all((got == want) | near_half)
     assert np.any(np.abs(ss[1].astype(int)) == 127) and np.mean(np.abs(ss[1].astype(int)) == 127) > 0.01
+
+
+# --------------------------------------------------------------------------- block size
+@pytest.mark.parametrize("bs", [1, 3, 100, 777, 4096])
+def test_quantize_any_block_size_brute_force(bs):
+    """BlockSize (PR #814 options: any positive size): each block of bs consecutive
+    elements, the last one partial, gets its own absmax scale; every code is the nearest
+    code under that scale by exhaustive search."""
+    n = 3 * bs + (bs // 2 if bs > 1 else 0) + 1
+    rng = np.random.default_rng(bs)
+    m = (rng.standard_normal(n) * 1e-3).astype(F32)
+    v = (rng.exponential(1.0, n) * 1e-6).astype(F32)
+    q8 = Q8Opts(block_size=bs)
+    mc, vc, ms, vs = oracle.quantize(m, v, q8)
+    nb = -(-n // bs)
+    assert ms.size == vs.size == nb
+    for b in range(nb):
+        sl = slice(b * bs, min(n, (b + 1) * bs))
+        for x, codes, s, lo, hi in ((m[sl], mc[sl], ms[b], -127, 127), (v[sl], vc[sl], vs[b], 0, 255)):
+            assert s == F32(np.abs(x).max()) / F32(hi)
+            ratio = x.astype(np.float64) / float(s)
+            near_half = np.abs(ratio - np.floor(ratio) - 0.5) < 2.0 ** -16
+            got = codes.astype(np.float64)
+            assert np.all((got == _brute_nearest(x, s, lo, hi)) | near_half)
+    # dequantize indexes scales by element // bs
+    dm, dv = oracle.dequantize(mc, vc, ms, vs, block_size=bs)
+    blk = np.arange(n) // bs
+    np.testing.assert_array_equal(dm, mc.astype(F32) * ms[blk])
+    np.testing.assert_array_equal(dv, vc.astype(F32) * vs[blk])
+
+
+def test_block_size_one_is_sign_and_magnitude():
+    """With one element per block the scale is |x|/qmax and every nonzero m codes to
+    +-127, every nonzero v to 255 (|x/s| = qmax within one rounding of s)."""
+    rng = np.random.default_rng(3)
+    m = (rng.standard_normal(1000) * 1e-3).astype(F32)
+    m[::97] = 0.0
+    v = (np.abs(rng.standard_normal(1000)) * 1e-6).astype(F32)
+    v[::89] = 0.0
+    mc, vc, ms, vs = oracle.quantize(m, v, Q8Opts(block_size=1))
+    np.testing.assert_array_equal(mc, (np.sign(m) * 127).astype(np.int8))
+    np.testing.assert_array_equal(vc, np.where(v > 0, 255, 0).astype(np.uint8))
+    np.testing.assert_array_equal(ms, np.abs(m) / F32(127))
+    np.testing.assert_array_equal(vs, v / F32(255))
+
+
+@pytest.mark.parametrize("bs", [64, 1000, 5000])
+def test_q8_step_any_block_size_is_dequantize_update_quantize(bs):
+    """The 8-bit step with block size bs is PR #814's diagram with that blocking: step 1
+    from zero state equals the fp32 step (params bit for bit, codes = quantize(m', v')),
+    and step 2 equals dequantize -> fp32 step -> quantize, all with block size bs."""
+    hp = HParams(weight_decay=0.01)
+    n = 2 * bs + bs // 3 + 5
+    p, g1 = _fresh(n, seed=bs)
+    q8 = Q8Opts(percentile=99.0, block_size=bs)
+    nb = oracle.n_blocks(n, bs)
+    st = [p.copy(), np.zeros(n, np.int8), np.zeros(n, np.uint8), np.zeros(nb, F32), np.zeros(nb, F32)]
+    pf, mf, vf = p.copy(), np.zeros_like(p), np.zeros_like(p)
+    oracle.step_fp32(pf, g1, mf, vf, 1, hp)
+    oracle.step_q8(*st[:1], g1, *st[1:], 1, hp, q8)
+    np.testing.assert_array_equal(st[0], pf)
+    for a, b in zip(st[1:], oracle.quantize(mf, vf, q8, step=1)):
+        np.testing.assert_array_equal(a, b)
+    _, g2 = _fresh(n, seed=bs + 1)
+    m1, v1 = oracle.dequantize(*st[1:], block_size=bs)
+    pf, mf, vf = st[0].copy(), m1, v1
+    oracle.step_fp32(pf, g2, mf, vf, 2, hp)
+    oracle.step_q8(*st[:1], g2, *st[1:], 2, hp, q8)
+    np.testing.assert_array_equal(st[0], pf)
+    for a, b in zip(st[1:], oracle.quantize(mf, vf, q8, step=2)):
+        np.testing.assert_array_equal(a, b)
+    # percentile 99 ranks within each block of bs (the last one partial): X_v is numpy's
+    # nearest-rank percentile of that block
+    for b in range(nb):
+        sl = slice(b * bs, min(n, (b + 1) * bs))
+        assert st[4][b] == F32(_np_nearest_rank(vf[sl], 99.0)) / F32(255)
+
+
+def test_q8v_step_any_block_size():
+    """fp32 m / 8-bit v with block size 300: m equals the fp32 step's m exactly and v's
+    codes and scales equal quantizing the fp32 step's v with that block size."""
+    hp = HParams(weight_decay=0.01)
+    bs, n = 300, 1000
+    p, g = _fresh(n, seed=77)
+    q8 = Q8Opts(block_size=bs)
+    nb = oracle.n_blocks(n, bs)
+    pq, m, vc, vs = p.copy(), np.zeros(n, F32), np.zeros(n, np.uint8), np.zeros(nb, F32)
+    pf, mf, vf = p.copy(), np.zeros_like(p), np.zeros_like(p)
+    oracle.step_fp32(pf, g, mf, vf, 1, hp)
+    oracle.step_q8v(pq, g, m, vc, vs, 1, hp, q8)
+    np.testing.assert_array_equal(pq, pf)
+    np.testing.assert_array_equal(m, mf)
+    _, vc2, _, vs2 = oracle.quantize(mf, vf, q8, step=1)
+    np.testing.assert_array_equal(vc, vc2)
+    np.testing.assert_array_equal(vs, vs2)
