@@ -12,8 +12,8 @@
  *
  * Sources of the method:
  *   - AiDotNet PR #814 "feat: add 8-bit Adam optimizer for memory efficiency":
- *     block-wise quantization with block size 2048, signed codes for m and unsigned
- *     codes for v, scales recomputed every step ("dynamic quantization"),
+ *     block-wise quantization with block size 2048 (options list: BlockSize, any
+ *     positive size), signed codes for m and unsigned codes for v, scales recomputed every step ("dynamic quantization"),
  *     QuantizationPercentile (default 99.9, range 0..100) for outlier-aware scaling,
  *     optional stochastic rounding; its sequence diagram fixes the step order:
  *     dequantize m and v, Adam update with bias correction, quantize m, quantize v.
@@ -30,7 +30,7 @@
  * (1-beta1), (1-beta2), 1 - lr*wd, lr/bc1 and 1/sqrt(bc2) are formed in double on the
  * host and rounded once to fp32. bf16 moments are widened exactly before and rounded to
  * nearest even after. 8-bit moments are decoded as code*scale, the update uses the
- * unquantized m', v', and each 2048-element block is then re-encoded:
+ * unquantized m', v', and each block of B elements (default 2048) is then re-encoded:
  *   X_m = k-th largest |m'| of the block, X_v = k-th largest v' (k = 1 for absmax)
  *   s_m = X_m / 127, s_v = X_v / 255  (if X = 0 the block's maximum is used instead)
  *   code = clamp(round(x / s), -127..127 for m, 0..255 for v); s = 0 gives code 0
@@ -44,8 +44,9 @@
  *   - Every device base pointer must be 16-byte aligned (PSADAM_ERR_MISALIGNED).
  *   - numel[i] >= 0; a tensor with numel 0 is skipped and its pointers may be NULL.
  *     n_tensors == 0 is a no-op.
- *   - Each tensor is split into consecutive 2048-element blocks; the last block may be
- *     partial. Scale arrays hold ceil(numel/2048) fp32 entries per tensor.
+ *   - Each tensor is split into consecutive blocks of B = block_size elements (2048 by
+ *     default); the last block may be partial. Scale arrays hold ceil(numel/B) fp32
+ *     entries per tensor.
  *   - step is the 1-based index of the step being taken (the caller increments it).
  *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default stream) and
  *     the call returns without synchronizing. Buffers must not alias one another.
@@ -69,7 +70,7 @@ typedef enum {
     PSADAM_OK = 0,
     PSADAM_ERR_INVALID_ARG = 1, /* NULL pointer, negative size, step < 1, bad hyper-parameter */
     PSADAM_ERR_MISALIGNED = 2,  /* a device base pointer is not 16-byte aligned */
-    PSADAM_ERR_UNSUPPORTED = 3, /* block size other than 2048, or a percentile rank above 16 */
+    PSADAM_ERR_UNSUPPORTED = 3, /* block size above 16384, or a block count above INT32_MAX */
     PSADAM_ERR_CUDA = 4         /* a kernel launch failed (see psadam_last_cuda_error) */
 } psadam_status;
 
@@ -85,13 +86,17 @@ typedef struct {
     float weight_decay; /* decoupled: p *= 1 - lr*weight_decay each step */
 } psadam_hparams;
 
-/* 8-bit options (PR #814's BlockSize, UseStochasticRounding, QuantizationPercentile). */
+/* 8-bit options (PR #814's BlockSize, UseStochasticRounding, QuantizationPercentile).
+ * Speed: block_size 2048 with a rank k <= 16 (percentile >= ~99.27, 100 included) runs the
+ * specialised 2048-block kernels; any other block size or a lower percentile runs a general
+ * kernel (one CTA per block, shared-memory staging, radix select) with identical results
+ * for identical inputs, only slower. */
 typedef struct {
-    int32_t block_size;          /* must be 2048, else PSADAM_ERR_UNSUPPORTED */
+    int32_t block_size;          /* elements per block, 1..16384 (INVALID_ARG below 1,
+                                    UNSUPPORTED above); PR #814's default is 2048 */
     int32_t stochastic_rounding; /* 0: round to nearest even; 1: Philox stochastic rounding */
     uint64_t seed;               /* Philox key (stochastic rounding only) */
-    float percentile;            /* (0, 100]; 100 = absmax. The block's rank k must be <= 16
-                                    (percentile >= ~99.27 for full blocks), else UNSUPPORTED */
+    float percentile;            /* (0, 100]; 100 = absmax */
     int32_t static_scales;       /* 0: scales recomputed every step (PR #814's default
                                     UseDynamicQuantization = true). 1: a block keeps its scale
                                     once it is nonzero (set by its first quantization); values
@@ -129,8 +134,8 @@ int adam_step_bf16m(const psadam_list* list, uint16_t* const* m, uint16_t* const
 
 /* One AdamW step with 8-bit block-wise moments (PR #814): dequantize, update and
  * requantize in one pass. m_code: device int8_t[numel] in [-127,127]; v_code: device
- * uint8_t[numel]; m_scale, v_scale: device float[ceil(numel/2048)]; all updated in
- * place. Fresh state is all zeros (codes 0, scales 0). Stochastic rounding of element e
+ * uint8_t[numel]; m_scale, v_scale: device float[ceil(numel/block_size)]; all updated
+ * in place. Fresh state is all zeros (codes 0, scales 0). Stochastic rounding of element e
  * of list tensor i draws word e%4 of Philox4x32-10(counter = (e/4 low, e/4 high,
  * step low 32 bits, 2*i + moment), key = seed), moment 0 for m and 1 for v; u is the
  * word's top 24 bits times 2^-24. */
@@ -141,7 +146,7 @@ int adam_step_q8(const psadam_list* list, int8_t* const* m_code, uint8_t* const*
 /* One AdamW step keeping the first moment in fp32 and only the second moment 8-bit (PR
  * #814's "Option to keep first moment in full precision (CompressBothMoments=false)").
  * m: device float[numel]; v_code: device uint8_t[numel]; v_scale: device
- * float[ceil(numel/2048)]; all updated in place. v is encoded exactly as adam_step_q8
+ * float[ceil(numel/block_size)]; all updated in place. v is encoded exactly as adam_step_q8
  * encodes it (same percentile rule, rounding and stochastic-rounding stream, moment 1). */
 int adam_step_q8v(const psadam_list* list, float* const* m, uint8_t* const* v_code, float* const* v_scale,
                   int64_t step, const psadam_hparams* hp, const psadam_q8_opts* q8, void* stream);
@@ -156,11 +161,12 @@ int psadam_q8_quantize(int32_t n_tensors, const int64_t* numel, const float* con
                        int64_t step, void* stream);
 
 /* Dequantize-only (PR #814's Dequantize): m = code*scale, v = code*scale (one fp32
- * multiply each) into device float m[numel], v[numel]. */
+ * multiply each, element e taking scale e / block_size) into device float m[numel],
+ * v[numel]. block_size as in psadam_q8_opts. */
 int psadam_q8_dequantize(int32_t n_tensors, const int64_t* numel, const int8_t* const* m_code,
                          const uint8_t* const* v_code, const float* const* m_scale,
                          const float* const* v_scale, float* const* m, float* const* v,
-                         void* stream);
+                         int32_t block_size, void* stream);
 
 /* Non-finite grad check (the "found inf" test of a mixed-precision step): writes 0 to the
  * device int32 *found_nonfinite, then 1 if any grad of the list, multiplied by
@@ -168,11 +174,11 @@ int psadam_q8_dequantize(int32_t n_tensors, const int64_t* numel, const int8_t* 
  * NULL). Pass the same flag as skip_if_set of the following step to skip it. */
 int psadam_check_grads(const psadam_list* list, int32_t* found_nonfinite, void* stream);
 
-/* Bytes of optimizer state for a tensor of numel params (PR #814's GetMemoryUsage):
- * mode 0 = fp32 (8*numel), 1 = bf16 (4*numel), 2 = 8-bit (2*numel + 8*ceil(numel/2048)),
- * 3 = fp32 m + 8-bit v (5*numel + 4*ceil(numel/2048)).
- * Returns 0 for an unknown mode or numel < 0. */
-size_t psadam_state_bytes(int32_t mode, int64_t numel);
+/* Bytes of optimizer state for a tensor of numel params (PR #814's GetMemoryUsage), B =
+ * block_size (ignored by modes 0 and 1): mode 0 = fp32 (8*numel), 1 = bf16 (4*numel),
+ * 2 = 8-bit (2*numel + 8*ceil(numel/B)), 3 = fp32 m + 8-bit v (5*numel + 4*ceil(numel/B)).
+ * Returns 0 for an unknown mode, numel < 0, or B < 1 in modes 2 and 3. */
+size_t psadam_state_bytes(int32_t mode, int64_t numel, int32_t block_size);
 
 /* Static, human-readable name of a psadam_status value. */
 const char* psadam_status_string(int32_t status);

@@ -11,7 +11,7 @@ Entry points (same names as the C ABI):
     adam_step_q8(params, grads, m_code, v_code, m_scale, v_scale, step, ...)
     adam_step_q8v(params, grads, m, v_code, v_scale, step, ...) fp32 m, 8-bit v
     q8_quantize / q8_dequantize                                 8-bit state conversion
-    state_bytes(mode, numel)                                    optimizer-state footprint
+    state_bytes(mode, numel, block_size)                        optimizer-state footprint
 and helpers to allocate fresh (zero) state with the right dtypes and shapes.
 """
 from __future__ import annotations
@@ -24,8 +24,9 @@ import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libpsadam.so")
-BLOCK = 2048
-MAX_PERCENTILE_RANK = 16
+BLOCK = 2048             # the 8-bit format's default block (the specialised kernels' size)
+MAX_BLOCK = 16384        # largest block size the library accepts
+MAX_PERCENTILE_RANK = 16 # above this rank (or at another block size) the general kernel runs
 
 OK, ERR_INVALID_ARG, ERR_MISALIGNED, ERR_UNSUPPORTED, ERR_CUDA = range(5)
 GRAD_F32, GRAD_BF16 = 0, 1
@@ -67,13 +68,13 @@ _SIGS = {
                       ctypes.POINTER(_Q8Opts), _vp],
     "psadam_q8_quantize": [ctypes.c_int32, _I64P, _PP, _PP, _PP, _PP, _PP, _PP, ctypes.POINTER(_Q8Opts),
                            ctypes.c_int64, _vp],
-    "psadam_q8_dequantize": [ctypes.c_int32, _I64P, _PP, _PP, _PP, _PP, _PP, _PP, _vp],
+    "psadam_q8_dequantize": [ctypes.c_int32, _I64P, _PP, _PP, _PP, _PP, _PP, _PP, ctypes.c_int32, _vp],
     "psadam_check_grads": [ctypes.POINTER(_List), _vp, _vp],
 }
 for _name, _args in _SIGS.items():
     getattr(_lib, _name).argtypes = _args
     getattr(_lib, _name).restype = ctypes.c_int
-_lib.psadam_state_bytes.argtypes = [ctypes.c_int32, ctypes.c_int64]
+_lib.psadam_state_bytes.argtypes = [ctypes.c_int32, ctypes.c_int64, ctypes.c_int32]
 _lib.psadam_state_bytes.restype = ctypes.c_size_t
 _lib.psadam_status_string.argtypes = [ctypes.c_int32]
 _lib.psadam_status_string.restype = ctypes.c_char_p
@@ -94,12 +95,16 @@ def status_string(status: int) -> str:
     return _lib.psadam_status_string(status).decode()
 
 
-def state_bytes(mode: str | int, numel: int) -> int:
-    return int(_lib.psadam_state_bytes(MODES.get(mode, mode) if isinstance(mode, str) else mode, numel))
+def state_bytes(mode: str | int, numel: int, block_size: int = BLOCK) -> int:
+    return int(_lib.psadam_state_bytes(MODES.get(mode, mode) if isinstance(mode, str) else mode, numel, block_size))
 
 
-def n_blocks(numel: int) -> int:
-    return (numel + BLOCK - 1) // BLOCK
+def n_blocks(numel: int, block_size: int = BLOCK) -> int:
+    return (numel + block_size - 1) // block_size
+
+
+def _nb(block_size: int):
+    return lambda n: n_blocks(n, block_size)
 
 
 # ------------------------------------------------------------------ marshalling
@@ -219,8 +224,8 @@ def adam_step_q8(params, grads, m_code, v_code, m_scale, v_scale, step: int, lr:
     lst, keep = _list(params, grads, grad_unscale, zero_grads, skip_flag)
     _check_layout("m_code", m_code, torch.int8, params)
     _check_layout("v_code", v_code, torch.uint8, params)
-    _check_layout("m_scale", m_scale, torch.float32, params, n_blocks)
-    _check_layout("v_scale", v_scale, torch.float32, params, n_blocks)
+    _check_layout("m_scale", m_scale, torch.float32, params, _nb(block_size))
+    _check_layout("v_scale", v_scale, torch.float32, params, _nb(block_size))
     ptrs = [_ptrs(x) for x in (m_code, v_code, m_scale, v_scale)]
     st = _lib.adam_step_q8(ctypes.byref(lst), *[ctypes.cast(p, _PP) for p in ptrs], step,
                            ctypes.byref(_hp(lr, beta1, beta2, eps, weight_decay)),
@@ -238,7 +243,7 @@ def adam_step_q8v(params, grads, m, v_code, v_scale, step: int, lr: float = 1e-3
     lst, keep = _list(params, grads, grad_unscale, zero_grads, skip_flag)
     _check_layout("m", m, torch.float32, params)
     _check_layout("v_code", v_code, torch.uint8, params)
-    _check_layout("v_scale", v_scale, torch.float32, params, n_blocks)
+    _check_layout("v_scale", v_scale, torch.float32, params, _nb(block_size))
     ptrs = [_ptrs(x) for x in (m, v_code, v_scale)]
     st = _lib.adam_step_q8v(ctypes.byref(lst), *[ctypes.cast(p, _PP) for p in ptrs], step,
                             ctypes.byref(_hp(lr, beta1, beta2, eps, weight_decay)),
@@ -264,8 +269,8 @@ def q8_quantize(m, v, m_code, v_code, m_scale, v_scale, step: int = 1, stochasti
     _check_layout("v", v, torch.float32, m)
     _check_layout("m_code", m_code, torch.int8, m)
     _check_layout("v_code", v_code, torch.uint8, m)
-    _check_layout("m_scale", m_scale, torch.float32, m, n_blocks)
-    _check_layout("v_scale", v_scale, torch.float32, m, n_blocks)
+    _check_layout("m_scale", m_scale, torch.float32, m, _nb(block_size))
+    _check_layout("v_scale", v_scale, torch.float32, m, _nb(block_size))
     ptrs = [_ptrs(x) for x in (m, v, m_code, v_code, m_scale, v_scale)]
     st = _lib.psadam_q8_quantize(len(m), _numels(m), *[ctypes.cast(p, _PP) for p in ptrs],
                                  ctypes.byref(_q8(stochastic_rounding, seed, percentile, block_size)), step,
@@ -273,25 +278,25 @@ def q8_quantize(m, v, m_code, v_code, m_scale, v_scale, step: int = 1, stochasti
     _raise(st, "psadam_q8_quantize")
 
 
-def q8_dequantize(m_code, v_code, m_scale, v_scale, m, v, stream=None) -> None:
+def q8_dequantize(m_code, v_code, m_scale, v_scale, m, v, block_size: int = BLOCK, stream=None) -> None:
     """Decode 8-bit codes and block scales into fp32 moments (code * scale)."""
     _check_layout("m_code", m_code, torch.int8)
     _check_layout("v_code", v_code, torch.uint8, m_code)
-    _check_layout("m_scale", m_scale, torch.float32, m_code, n_blocks)
-    _check_layout("v_scale", v_scale, torch.float32, m_code, n_blocks)
+    _check_layout("m_scale", m_scale, torch.float32, m_code, _nb(block_size))
+    _check_layout("v_scale", v_scale, torch.float32, m_code, _nb(block_size))
     _check_layout("m", m, torch.float32, m_code)
     _check_layout("v", v, torch.float32, m_code)
     ptrs = [_ptrs(x) for x in (m_code, v_code, m_scale, v_scale, m, v)]
-    st = _lib.psadam_q8_dequantize(len(m_code), _numels(m_code), *[ctypes.cast(p, _PP) for p in ptrs],
+    st = _lib.psadam_q8_dequantize(len(m_code), _numels(m_code), *[ctypes.cast(p, _PP) for p in ptrs], block_size,
                                    _stream_handle(stream, m))
     _raise(st, "psadam_q8_dequantize")
 
 
 # ------------------------------------------------------------------ state allocation (caller side)
-def zeros_state(params, mode: str):
+def zeros_state(params, mode: str, block_size: int = BLOCK):
     """Fresh (all-zero) optimizer state for ``params`` in moment mode ``mode``.
     fp32/bf16m: (m list, v list); q8: (m_code, v_code, m_scale, v_scale) lists;
-    q8v: (m fp32, v_code, v_scale) lists."""
+    q8v: (m fp32, v_code, v_scale) lists (one scale per ``block_size`` elements)."""
     if mode == "fp32":
         return [torch.zeros_like(p) for p in params], [torch.zeros_like(p) for p in params]
     if mode == "bf16m":
@@ -300,12 +305,12 @@ def zeros_state(params, mode: str):
     if mode == "q8":
         return ([torch.zeros(p.numel(), dtype=torch.int8, device=p.device) for p in params],
                 [torch.zeros(p.numel(), dtype=torch.uint8, device=p.device) for p in params],
-                [torch.zeros(n_blocks(p.numel()), dtype=torch.float32, device=p.device) for p in params],
-                [torch.zeros(n_blocks(p.numel()), dtype=torch.float32, device=p.device) for p in params])
+                [torch.zeros(n_blocks(p.numel(), block_size), dtype=torch.float32, device=p.device) for p in params],
+                [torch.zeros(n_blocks(p.numel(), block_size), dtype=torch.float32, device=p.device) for p in params])
     if mode == "q8v":
         return ([torch.zeros_like(p) for p in params],
                 [torch.zeros(p.numel(), dtype=torch.uint8, device=p.device) for p in params],
-                [torch.zeros(n_blocks(p.numel()), dtype=torch.float32, device=p.device) for p in params])
+                [torch.zeros(n_blocks(p.numel(), block_size), dtype=torch.float32, device=p.device) for p in params])
     raise ValueError(f"unknown moment mode {mode!r}")
 
 
@@ -353,12 +358,12 @@ class StepPlan:
         elif mode == "q8":
             _check_layout("m_code", state[0], torch.int8, params)
             _check_layout("v_code", state[1], torch.uint8, params)
-            _check_layout("m_scale", state[2], torch.float32, params, n_blocks)
-            _check_layout("v_scale", state[3], torch.float32, params, n_blocks)
+            _check_layout("m_scale", state[2], torch.float32, params, _nb(block_size))
+            _check_layout("v_scale", state[3], torch.float32, params, _nb(block_size))
         else:
             _check_layout("m", state[0], torch.float32, params)
             _check_layout("v_code", state[1], torch.uint8, params)
-            _check_layout("v_scale", state[2], torch.float32, params, n_blocks)
+            _check_layout("v_scale", state[2], torch.float32, params, _nb(block_size))
         self._state_ptrs = [_ptrs(x) for x in state]
         self._state_pp = [ctypes.cast(p, _PP) for p in self._state_ptrs]
         self._state = state

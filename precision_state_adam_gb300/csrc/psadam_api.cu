@@ -43,9 +43,16 @@ int check_hparams(const psadam_hparams* hp, int64_t step) {
   return PSADAM_OK;
 }
 
+int check_block_size(int32_t bs) {
+  if (bs < 1) return PSADAM_ERR_INVALID_ARG;
+  if (bs > kMaxAnyBlock) return PSADAM_ERR_UNSUPPORTED;
+  return PSADAM_OK;
+}
+
 int check_q8(const psadam_q8_opts* q) {
   if (!q) return PSADAM_ERR_INVALID_ARG;
-  if (q->block_size != kBlock) return PSADAM_ERR_UNSUPPORTED;
+  const int st = check_block_size(q->block_size);
+  if (st != PSADAM_OK) return st;
   if (q->stochastic_rounding != 0 && q->stochastic_rounding != 1) return PSADAM_ERR_INVALID_ARG;
   if (!finite(q->percentile) || !(q->percentile > 0.f) || q->percentile > 100.f) return PSADAM_ERR_INVALID_ARG;
   if (q->static_scales != 0 && q->static_scales != 1) return PSADAM_ERR_INVALID_ARG;
@@ -80,8 +87,8 @@ int percentile_rank(float pct, long long n) {
   return (int)k;
 }
 
-long long n_blocks(long long n) { return (n + kBlock - 1) / kBlock; }
-int last_block_len(long long n) { return (int)(n - (n_blocks(n) - 1) * kBlock); }
+long long n_blocks(long long n, int bs = kBlock) { return (n + bs - 1) / bs; }
+int last_block_len(long long n, int bs = kBlock) { return (int)(n - (n_blocks(n, bs) - 1) * bs); }
 
 // Validate one tensor's pointers. `ptrs` lists the ones that must be present.
 int check_tensor(long long numel, std::initializer_list<const void*> ptrs) {
@@ -96,13 +103,20 @@ int check_tensor(long long numel, std::initializer_list<const void*> ptrs) {
 }
 
 // Highest percentile rank any block of the list needs.
-int max_rank(const std::vector<Entry>& es, float pct) {
+int max_rank(const std::vector<Entry>& es, float pct, int bs) {
   int k = 1;
   for (const Entry& e : es) {
-    if (e.numel >= kBlock) k = std::max(k, percentile_rank(pct, kBlock));
-    k = std::max(k, percentile_rank(pct, last_block_len(e.numel)));
+    if (e.numel >= bs) k = std::max(k, percentile_rank(pct, bs));
+    k = std::max(k, percentile_rank(pct, last_block_len(e.numel, bs)));
   }
   return k;
+}
+
+// Every tensor's block count must fit a grid dimension.
+int check_block_counts(const std::vector<Entry>& es, int bs) {
+  for (const Entry& e : es)
+    if (n_blocks(e.numel, bs) > INT_MAX) return PSADAM_ERR_UNSUPPORTED;
+  return PSADAM_OK;
 }
 
 template <int CAP>
@@ -119,7 +133,7 @@ struct GradSide {
 // Pack the list into as few launches as fit and run `fn` on each.
 template <int CAP, typename Fn>
 int run_launches(const std::vector<Entry>& es, const StepConsts& c, uint64_t seed, int64_t step, float pct,
-                 const GradSide& gs, Fn fn, cudaStream_t stream) {
+                 const GradSide& gs, Fn fn, cudaStream_t stream, int bs = kBlock) {
   static thread_local LaunchArgs<CAP> a;  // ~32 KB: keep it off the stack
   std::memset(&a, 0, sizeof a);
   a.c = c;
@@ -130,13 +144,14 @@ int run_launches(const std::vector<Entry>& es, const StepConsts& c, uint64_t see
   a.seed_lo = (uint32_t)(seed & 0xFFFFFFFFu);
   a.seed_hi = (uint32_t)(seed >> 32);
   a.step_lo = (uint32_t)step;
-  a.k_full = percentile_rank(pct, kBlock);
+  a.block_size = bs;
+  a.k_full = percentile_rank(pct, bs);
   size_t i = 0;
   while (i < es.size()) {
     int nt = 0;
     long long blocks = 0;
     while (i < es.size() && nt < CAP) {
-      const long long nb = n_blocks(es[i].numel);
+      const long long nb = n_blocks(es[i].numel, bs);
       if (blocks + nb > INT_MAX) break;
       TensorRef& t = a.t[nt++];
       t.p = es[i].p;
@@ -147,7 +162,7 @@ int run_launches(const std::vector<Entry>& es, const StepConsts& c, uint64_t see
       t.vs = es[i].vs;
       t.numel = es[i].numel;
       t.block_begin = (int)blocks;
-      t.k_last = percentile_rank(pct, last_block_len(es[i].numel));
+      t.k_last = percentile_rank(pct, last_block_len(es[i].numel, bs));
       t.list_idx = es[i].list_idx;
       blocks += nb;
       ++i;
@@ -186,6 +201,16 @@ Launcher<CAP> pick_step(int mode, bool gb, bool sr, int K) {
 }
 
 template <int CAP>
+Launcher<CAP> pick_step_any(int mode, bool gb, bool sr) {
+  if (mode == kModeQ8V) {
+    if (gb) return sr ? &launch_step_any<kModeQ8V, true, true, CAP> : &launch_step_any<kModeQ8V, true, false, CAP>;
+    return sr ? &launch_step_any<kModeQ8V, false, true, CAP> : &launch_step_any<kModeQ8V, false, false, CAP>;
+  }
+  if (gb) return sr ? &launch_step_any<kModeQ8, true, true, CAP> : &launch_step_any<kModeQ8, true, false, CAP>;
+  return sr ? &launch_step_any<kModeQ8, false, true, CAP> : &launch_step_any<kModeQ8, false, false, CAP>;
+}
+
+template <int CAP>
 Launcher<CAP> pick_quantize(bool sr, int K) {
   if (sr) return K == 1 ? &launch_quantize<true, 1, CAP> : (K == 4 ? &launch_quantize<true, 4, CAP> : &launch_quantize<true, 16, CAP>);
   return K == 1 ? &launch_quantize<false, 1, CAP> : (K == 4 ? &launch_quantize<false, 4, CAP> : &launch_quantize<false, 16, CAP>);
@@ -194,10 +219,10 @@ Launcher<CAP> pick_quantize(bool sr, int K) {
 // Dispatch on list length: short lists use the small parameter block.
 int dispatch(const std::vector<Entry>& es, const StepConsts& c, uint64_t seed, int64_t step, float pct,
              Launcher<kCapSmall> small, Launcher<kCapLarge> large, cudaStream_t stream,
-             const GradSide& gs = GradSide{}) {
+             const GradSide& gs = GradSide{}, int bs = kBlock) {
   if (es.empty()) return PSADAM_OK;
-  if (es.size() <= (size_t)kCapSmall) return run_launches<kCapSmall>(es, c, seed, step, pct, gs, small, stream);
-  return run_launches<kCapLarge>(es, c, seed, step, pct, gs, large, stream);
+  if (es.size() <= (size_t)kCapSmall) return run_launches<kCapSmall>(es, c, seed, step, pct, gs, small, stream, bs);
+  return run_launches<kCapLarge>(es, c, seed, step, pct, gs, large, stream, bs);
 }
 
 // The list's grad-side options; 0 as an unscale factor reads as 1 (a zeroed struct changes nothing).
@@ -248,16 +273,22 @@ int step_common(int mode, const psadam_list* list, const void* const* m, const v
   const float pct = q8mode ? q8->percentile : 100.f;
   const bool sr = q8mode && q8->stochastic_rounding;
   const uint64_t seed = q8mode ? q8->seed : 0;
-  const int kmax = max_rank(es, pct);
-  if (kmax > kMaxRank) return PSADAM_ERR_UNSUPPORTED;
+  const int bs = q8mode ? q8->block_size : kBlock;
+  if ((st = check_block_counts(es, bs)) != PSADAM_OK) return st;
+  const int kmax = max_rank(es, pct, bs);
   GradSide gs;
   if ((st = grad_side(list, gs)) != PSADAM_OK) return st;
   gs.static_scales = q8mode && q8->static_scales != 0;
-  const int K = rank_template(kmax);
   const bool gb = list->grad_dtype == PSADAM_GRAD_BF16;
   const StepConsts c = make_consts(*hp, step);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // 2048-element blocks with rank <= 16: the specialised kernels; otherwise one CTA per block
+  if (q8mode && (bs != kBlock || kmax > kMaxRank))
+    return dispatch(es, c, seed, step, pct, pick_step_any<kCapSmall>(mode, gb, sr), pick_step_any<kCapLarge>(mode, gb, sr),
+                    s, gs, bs);
+  const int K = rank_template(kmax);
   return dispatch(es, c, seed, step, pct, pick_step<kCapSmall>(mode, gb, sr, K), pick_step<kCapLarge>(mode, gb, sr, K),
-                  static_cast<cudaStream_t>(stream), gs);
+                  s, gs);
 }
 
 }  // namespace
@@ -306,19 +337,28 @@ int psadam_q8_quantize(int32_t n_tensors, const int64_t* numel, const float* con
     es.push_back(Entry{reinterpret_cast<float*>(m_code[i]), v_code[i], const_cast<float*>(m[i]),
                        const_cast<float*>(v[i]), m_scale[i], v_scale[i], numel[i], i});
   }
-  const int kmax = max_rank(es, q8->percentile);
-  if (kmax > kMaxRank) return PSADAM_ERR_UNSUPPORTED;
-  const int K = rank_template(kmax);
+  const int bs = q8->block_size;
+  if ((st = check_block_counts(es, bs)) != PSADAM_OK) return st;
+  const int kmax = max_rank(es, q8->percentile, bs);
   const bool sr = q8->stochastic_rounding != 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (bs != kBlock || kmax > kMaxRank)
+    return dispatch(es, StepConsts{}, q8->seed, step, q8->percentile,
+                    sr ? &launch_quantize_any<true, kCapSmall> : &launch_quantize_any<false, kCapSmall>,
+                    sr ? &launch_quantize_any<true, kCapLarge> : &launch_quantize_any<false, kCapLarge>, s, GradSide{},
+                    bs);
+  const int K = rank_template(kmax);
   return dispatch(es, StepConsts{}, q8->seed, step, q8->percentile, pick_quantize<kCapSmall>(sr, K),
-                  pick_quantize<kCapLarge>(sr, K), static_cast<cudaStream_t>(stream));
+                  pick_quantize<kCapLarge>(sr, K), s);
 }
 
 int psadam_q8_dequantize(int32_t n_tensors, const int64_t* numel, const int8_t* const* m_code,
                          const uint8_t* const* v_code, const float* const* m_scale, const float* const* v_scale,
-                         float* const* m, float* const* v, void* stream) {
+                         float* const* m, float* const* v, int32_t block_size, void* stream) {
   if (n_tensors < 0) return PSADAM_ERR_INVALID_ARG;
   if (n_tensors == 0) return PSADAM_OK;
+  const int bst = check_block_size(block_size);
+  if (bst != PSADAM_OK) return bst;
   if (!numel || !m || !v || !m_code || !v_code || !m_scale || !v_scale) return PSADAM_ERR_INVALID_ARG;
   std::vector<Entry> es;
   for (int i = 0; i < n_tensors; ++i) {
@@ -328,8 +368,12 @@ int psadam_q8_dequantize(int32_t n_tensors, const int64_t* numel, const int8_t* 
     es.push_back(Entry{reinterpret_cast<float*>(const_cast<int8_t*>(m_code[i])), v_code[i], m[i], v[i],
                        const_cast<float*>(m_scale[i]), const_cast<float*>(v_scale[i]), numel[i], i});
   }
-  return dispatch(es, StepConsts{}, 0, 1, 100.f, &launch_dequantize<kCapSmall>, &launch_dequantize<kCapLarge>,
-                  static_cast<cudaStream_t>(stream));
+  if (check_block_counts(es, block_size) != PSADAM_OK) return PSADAM_ERR_UNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (block_size != kBlock)
+    return dispatch(es, StepConsts{}, 0, 1, 100.f, &launch_dequantize_any<kCapSmall>, &launch_dequantize_any<kCapLarge>,
+                    s, GradSide{}, block_size);
+  return dispatch(es, StepConsts{}, 0, 1, 100.f, &launch_dequantize<kCapSmall>, &launch_dequantize<kCapLarge>, s);
 }
 
 int psadam_check_grads(const psadam_list* list, int32_t* found_nonfinite, void* stream) {
@@ -365,14 +409,15 @@ int psadam_check_grads(const psadam_list* list, int32_t* found_nonfinite, void* 
   return run_launches<kCapLarge>(es, StepConsts{}, 0, 1, 100.f, gs, large, s);
 }
 
-size_t psadam_state_bytes(int32_t mode, int64_t numel) {
+size_t psadam_state_bytes(int32_t mode, int64_t numel, int32_t block_size) {
   if (numel < 0) return 0;
   const size_t n = (size_t)numel;
+  if ((mode == 2 || mode == 3) && block_size < 1) return 0;
   switch (mode) {
     case 0: return 8 * n;
     case 1: return 4 * n;
-    case 2: return 2 * n + 8 * (size_t)n_blocks(numel);
-    case 3: return 5 * n + 4 * (size_t)n_blocks(numel);
+    case 2: return 2 * n + 8 * (size_t)n_blocks(numel, block_size);
+    case 3: return 5 * n + 4 * (size_t)n_blocks(numel, block_size);
     default: return 0;
   }
 }

@@ -17,7 +17,10 @@ constexpr int kWarps = kThreads / 32;
 // long lists the largest block that stays under the 32,764-byte parameter limit.
 constexpr int kCapSmall = 8;
 constexpr int kCapLarge = 440;
-constexpr int kMaxRank = 16;  // largest percentile rank k the 8-bit kernels select
+constexpr int kMaxRank = 16;  // largest percentile rank k the 2048-block kernels select
+// Largest quantization block of the any-block-size kernels (its fp32 m', v' are staged in
+// shared memory: 128 KB for both moments).
+constexpr int kMaxAnyBlock = 16384;
 
 enum Mode : int { kModeF32 = 0, kModeBF16 = 1, kModeQ8 = 2, kModeQ8V = 3 };  // Q8V: fp32 m, 8-bit v
 
@@ -54,7 +57,7 @@ struct LaunchArgs {
   int zero_grads;   // nonzero: overwrite each grad with zero after reading it
   const int* skip;  // device flag or null: a nonzero value makes the launch a no-op
   int static_scales;  // 8-bit: a block's nonzero scale is kept instead of recomputed
-  int pad_;
+  int block_size;     // 8-bit quantization block (the 2048-block kernels assume 2048)
   TensorRef t[CAP];
 };
 static_assert(sizeof(LaunchArgs<kCapLarge>) <= 32764, "kernel parameter block too large");
@@ -71,6 +74,16 @@ cudaError_t launch_quantize(const LaunchArgs<CAP>& a, cudaStream_t s);
 
 template <int CAP>
 cudaError_t launch_dequantize(const LaunchArgs<CAP>& a, cudaStream_t s);
+
+// Any block size in [1, kMaxAnyBlock] and any percentile rank: one CTA per quantization block.
+template <int MODE, bool GBF16, bool SR, int CAP>
+cudaError_t launch_step_any(const LaunchArgs<CAP>& a, cudaStream_t s);
+
+template <bool SR, int CAP>
+cudaError_t launch_quantize_any(const LaunchArgs<CAP>& a, cudaStream_t s);
+
+template <int CAP>
+cudaError_t launch_dequantize_any(const LaunchArgs<CAP>& a, cudaStream_t s);
 
 // Non-finite grad check: sets *flag = 1 if any grad (times g_unscale) is inf or NaN.
 template <bool GBF16, int CAP>

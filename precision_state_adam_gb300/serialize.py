@@ -28,7 +28,8 @@ import torch
 
 MAGIC = b"PSADAMST"
 VERSION = 1
-BLOCK = 2048
+BLOCK = 2048       # default 8-bit block size
+MAX_BLOCK = 16384  # largest block size the library accepts
 
 # per mode: the state tensors of one parameter tensor, as (name, dtype, count kind)
 _LAYOUT = {
@@ -46,8 +47,8 @@ class StateFormatError(ValueError):
     pass
 
 
-def _count(kind: str, n: int) -> int:
-    return n if kind == "n" else (n + BLOCK - 1) // BLOCK
+def _count(kind: str, n: int, bs: int) -> int:
+    return n if kind == "n" else (n + bs - 1) // bs
 
 
 def _raw(t: torch.Tensor) -> bytes:
@@ -58,11 +59,13 @@ def _raw(t: torch.Tensor) -> bytes:
 
 
 def save_state(f: str | BinaryIO, mode: str, state, step: int, hparams: dict | None = None,
-               q8: dict | None = None) -> None:
-    """Write ``state`` (as returned by ``zeros_state(params, mode)``), the number of steps
-    taken, and optionally the hyper-parameters and 8-bit options."""
+               q8: dict | None = None, block_size: int = BLOCK) -> None:
+    """Write ``state`` (as returned by ``zeros_state(params, mode, block_size)``), the number
+    of steps taken, and optionally the hyper-parameters and 8-bit options."""
     if mode not in _LAYOUT:
         raise ValueError(f"unknown moment mode {mode!r}")
+    if not 1 <= block_size <= MAX_BLOCK:
+        raise ValueError(f"block size {block_size} outside 1..{MAX_BLOCK}")
     layout = _LAYOUT[mode]
     if len(state) != len(layout):
         raise ValueError(f"{mode} state has {len(layout)} parts, got {len(state)}")
@@ -71,13 +74,13 @@ def save_state(f: str | BinaryIO, mode: str, state, step: int, hparams: dict | N
     for i, n in enumerate(numel):
         for (name, dtype, kind), part in zip(layout, state):
             t = part[i]
-            if t.dtype != dtype or t.numel() != _count(kind, n):
-                raise ValueError(f"tensor {i} {name}: expected {_count(kind, n)} x {dtype}, "
+            if t.dtype != dtype or t.numel() != _count(kind, n, block_size):
+                raise ValueError(f"tensor {i} {name}: expected {_count(kind, n, block_size)} x {dtype}, "
                                  f"got {t.numel()} x {t.dtype}")
             arrays.append([f"{i}.{name}", _DTYPE_NAME[dtype], t.numel()])
             blobs.append(_raw(t))
     header = {
-        "mode": mode, "step": int(step), "block_size": BLOCK,
+        "mode": mode, "step": int(step), "block_size": int(block_size),
         "compress_both_moments": mode == "q8", "has_v_quantized": mode in ("q8", "q8v"),
         "hparams": hparams or {}, "q8": q8 or {}, "numel": numel, "arrays": arrays,
     }
@@ -105,8 +108,9 @@ def load_state(f: str | BinaryIO, device=None):
         raise StateFormatError(f"unsupported format version {version}")
     header = json.loads(data[16:16 + hlen].decode())
     mode = header["mode"]
-    if mode not in _LAYOUT or header.get("block_size") != BLOCK:
-        raise StateFormatError(f"unsupported mode / block size: {mode}, {header.get('block_size')}")
+    bs = header.get("block_size")
+    if mode not in _LAYOUT or not isinstance(bs, int) or not 1 <= bs <= MAX_BLOCK:
+        raise StateFormatError(f"unsupported mode / block size: {mode}, {bs}")
     if header["compress_both_moments"] != (mode == "q8") or header["has_v_quantized"] != (mode in ("q8", "q8v")):
         raise StateFormatError("flags disagree with the moment mode")
     layout = _LAYOUT[mode]
@@ -116,7 +120,7 @@ def load_state(f: str | BinaryIO, device=None):
     for i, n in enumerate(header["numel"]):
         for j, (name, dtype, kind) in enumerate(layout):
             aname, dname, count = next(it)
-            if aname != f"{i}.{name}" or _NAME_DTYPE.get(dname) != dtype or count != _count(kind, n):
+            if aname != f"{i}.{name}" or _NAME_DTYPE.get(dname) != dtype or count != _count(kind, n, bs):
                 raise StateFormatError(f"array {aname} does not match the {mode} layout")
             size = count * (2 if dtype == torch.bfloat16 else torch.empty(0, dtype=dtype).element_size())
             raw = bytearray(data[off:off + size])

@@ -54,16 +54,16 @@ def bf16_from_bits(a: np.ndarray, device) -> torch.Tensor:
     return torch.from_numpy(a.view(np.int16).copy()).to(device).view(torch.bfloat16)
 
 
-def host_state(mode: str, sizes):
+def host_state(mode: str, sizes, block_size: int = oracle.BLOCK):
     if mode == "fp32":
         return [(np.zeros(n, np.float32), np.zeros(n, np.float32)) for n in sizes]
     if mode == "bf16m":
         return [(np.zeros(n, np.uint16), np.zeros(n, np.uint16)) for n in sizes]
+    nb = lambda n: oracle.n_blocks(n, block_size)
     if mode == "q8v":
-        return [(np.zeros(n, np.float32), np.zeros(n, np.uint8), np.zeros(oracle.n_blocks(n), np.float32))
-                for n in sizes]
-    return [(np.zeros(n, np.int8), np.zeros(n, np.uint8), np.zeros(oracle.n_blocks(n), np.float32),
-             np.zeros(oracle.n_blocks(n), np.float32)) for n in sizes]
+        return [(np.zeros(n, np.float32), np.zeros(n, np.uint8), np.zeros(nb(n), np.float32)) for n in sizes]
+    return [(np.zeros(n, np.int8), np.zeros(n, np.uint8), np.zeros(nb(n), np.float32), np.zeros(nb(n), np.float32))
+            for n in sizes]
 
 
 def device_state_to_host(mode: str, state, i: int):
@@ -74,7 +74,7 @@ def device_state_to_host(mode: str, state, i: int):
     return tuple(s[i].cpu().numpy() for s in state)
 
 
-def compare_state(mode: str, got, want, what: str):
+def compare_state(mode: str, got, want, what: str, block_size: int = oracle.BLOCK):
     if mode == "fp32":
         assert_moment(got[0], want[0], what + " m")
         assert_moment(got[1], want[1], what + " v")
@@ -90,14 +90,14 @@ def compare_state(mode: str, got, want, what: str):
         assert_codes(got[1], want[1], what + " v codes")
         assert_moment(got[2], want[2], what + " v scales")
         same = got[1] == want[1]
-        gv = got[1].astype(np.float32) * np.repeat(got[2], 2048)[: got[1].size]
-        wv = want[1].astype(np.float32) * np.repeat(want[2], 2048)[: want[1].size]
+        gv = got[1].astype(np.float32) * np.repeat(got[2], block_size)[: got[1].size]
+        wv = want[1].astype(np.float32) * np.repeat(want[2], block_size)[: want[1].size]
         assert_moment(gv[same], wv[same], what + " v (dequantized)")
     else:
         assert_codes(got[0], want[0], what + " m codes")
         assert_codes(got[1], want[1], what + " v codes")
-        gm, gv = oracle.dequantize(*got)
-        wm, wv = oracle.dequantize(*want)
+        gm, gv = oracle.dequantize(*got, block_size=block_size)
+        wm, wv = oracle.dequantize(*want, block_size=block_size)
         # a code off by one moves its value by one scale step: compare where codes agree
         same_m = got[0] == want[0]
         same_v = got[1] == want[1]
@@ -120,7 +120,8 @@ def hp_kwargs(hp: HParams) -> dict:
 
 
 def q8_kwargs(q8: Q8Opts, step: bool = True) -> dict:
-    kw = dict(stochastic_rounding=q8.stochastic_rounding, seed=q8.seed, percentile=q8.percentile)
+    kw = dict(stochastic_rounding=q8.stochastic_rounding, seed=q8.seed, percentile=q8.percentile,
+              block_size=q8.block_size)
     if step:
         kw["static_scales"] = q8.static_scales
     return kw

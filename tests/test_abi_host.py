@@ -47,15 +47,19 @@ def test_library_does_not_link_the_oracle(psa):
 
 def test_state_bytes_closed_form(psa):
     lib = psa.cdll()
-    for n in (0, 1, 2047, 2048, 2049, 1 << 24, 86_564_352):
-        nb = -(-n // 2048)
-        assert lib.psadam_state_bytes(0, n) == 8 * n
-        assert lib.psadam_state_bytes(1, n) == 4 * n
-        assert lib.psadam_state_bytes(2, n) == 2 * n + 8 * nb
-        assert lib.psadam_state_bytes(3, n) == 5 * n + 4 * nb
-    assert lib.psadam_state_bytes(4, 10) == 0 and lib.psadam_state_bytes(0, -1) == 0
+    for bs in (2048, 1, 64, 1000, 16384):
+        for n in (0, 1, 2047, 2048, 2049, 1 << 24, 86_564_352):
+            nb = -(-n // bs)
+            assert lib.psadam_state_bytes(0, n, bs) == 8 * n
+            assert lib.psadam_state_bytes(1, n, bs) == 4 * n
+            assert lib.psadam_state_bytes(2, n, bs) == 2 * n + 8 * nb
+            assert lib.psadam_state_bytes(3, n, bs) == 5 * n + 4 * nb
+    assert lib.psadam_state_bytes(4, 10, 2048) == 0 and lib.psadam_state_bytes(0, -1, 2048) == 0
+    assert lib.psadam_state_bytes(2, 10, 0) == 0 and lib.psadam_state_bytes(3, 10, -1) == 0
+    assert lib.psadam_state_bytes(0, 10, 0) == 80  # block size only matters to 8-bit modes
     n = 1 << 24
-    assert 3.99 < lib.psadam_state_bytes(0, n) / lib.psadam_state_bytes(2, n) < 4.0
+    assert 3.99 < lib.psadam_state_bytes(0, n, 2048) / lib.psadam_state_bytes(2, n, 2048) < 4.0
+    assert psa.state_bytes("q8", 4096, 64) == 2 * 4096 + 8 * 64
 
 
 def test_status_strings(psa):
@@ -95,19 +99,21 @@ def test_validation_errors(psa):
     assert _call_q8(psa, numel=(-1,)) == E.ERR_INVALID_ARG
     assert _call_q8(psa, ptr=FAKE + 4) == E.ERR_MISALIGNED
     assert _call_q8(psa, ptr=0) == E.ERR_INVALID_ARG
-    assert _call_q8(psa, block=1024) == E.ERR_UNSUPPORTED
+    assert _call_q8(psa, block=0) == E.ERR_INVALID_ARG
+    assert _call_q8(psa, block=-64) == E.ERR_INVALID_ARG
+    assert _call_q8(psa, block=16385) == E.ERR_UNSUPPORTED          # beyond the staged block
     assert _call_q8(psa, pct=0.0) == E.ERR_INVALID_ARG
     assert _call_q8(psa, pct=100.5) == E.ERR_INVALID_ARG
     assert _call_q8(psa, pct=float("nan")) == E.ERR_INVALID_ARG
-    assert _call_q8(psa, pct=90.0) == E.ERR_UNSUPPORTED             # rank 205 of a full block
     assert _call_q8(psa, sr=2) == E.ERR_INVALID_ARG
     assert _call_q8(psa, grad_dtype=5) == E.ERR_INVALID_ARG
     for bad in ((1e-3, 1.0, 0.999, 1e-8, 0.0), (1e-3, 0.9, -0.1, 1e-8, 0.0), (float("inf"), 0.9, 0.999, 1e-8, 0.0),
                 (1e-3, 0.9, 0.999, -1.0, 0.0)):
         assert _call_q8(psa, hp=psa._HParams(*bad)) == E.ERR_INVALID_ARG
     assert psa.cdll().adam_step_q8(None, None, None, None, None, 1, None, None, None) == E.ERR_INVALID_ARG
-    # numel beyond what one grid can cover
+    # numel beyond what one grid can cover, at the default and at a small block size
     assert _call_q8(psa, numel=((2 ** 31) * 2048,)) == E.ERR_UNSUPPORTED
+    assert _call_q8(psa, numel=(2 ** 31,), block=1) == E.ERR_UNSUPPORTED
 
 
 def test_grad_side_validation(psa):
@@ -128,7 +134,10 @@ def test_grad_side_validation(psa):
     assert lib.psadam_check_grads(None, FAKE, None) == psa.ERR_INVALID_ARG
 
 
-def test_percentile_rank_limit_follows_the_block(psa):
-    # 99.0 -> rank 21 of a full block: beyond the selectable 16, rejected before launch
-    assert _call_q8(psa, numel=(2048,), pct=99.0) == psa.ERR_UNSUPPORTED
-    assert _call_q8(psa, numel=(5, 2048), pct=99.2) == psa.ERR_UNSUPPORTED  # rank 17
+def test_dequantize_block_size_validation(psa):
+    nums = _arr(ctypes.c_int64, [4096])
+    P = ctypes.cast(_arr(ctypes.c_void_p, [FAKE]), psa._PP)
+    lib = psa.cdll()
+    assert lib.psadam_q8_dequantize(1, nums, P, P, P, P, P, P, 0, None) == psa.ERR_INVALID_ARG
+    assert lib.psadam_q8_dequantize(1, nums, P, P, P, P, P, P, 16385, None) == psa.ERR_UNSUPPORTED
+    assert lib.psadam_q8_dequantize(0, nums, P, P, P, P, P, P, 0, None) == psa.OK  # empty list: no-op

@@ -60,8 +60,8 @@ def run_both(psa, mode, sizes, steps, hp, q8=Q8Opts(), grad_dtype="f32", grad_ki
     specs = [workloads.TensorSpec(f"t{i}", (n,)) for i, n in enumerate(sizes)]
     p_host = workloads.init_params_np(specs, seed=seed)
     params = _to_dev(p_host)
-    ostate = host_state(mode, sizes) if init_state is None else init_state
-    state = psa.zeros_state(params, mode)
+    ostate = host_state(mode, sizes, q8.block_size) if init_state is None else init_state
+    state = psa.zeros_state(params, mode, q8.block_size)
     if init_state is not None:
         for k, arrs in enumerate(zip(*init_state)):
             for i, a in enumerate(arrs):
@@ -81,11 +81,11 @@ def run_both(psa, mode, sizes, steps, hp, q8=Q8Opts(), grad_dtype="f32", grad_ki
     return got_p, p_host, got_s, ostate
 
 
-def check_all(mode, got_p, want_p, got_s, want_s, what):
+def check_all(mode, got_p, want_p, got_s, want_s, what, block_size=oracle.BLOCK):
     exact = []
     for i in range(len(got_p)):
         assert_params(got_p[i], want_p[i], f"{what} tensor {i}")
-        compare_state(mode, got_s[i], want_s[i], f"{what} tensor {i}")
+        compare_state(mode, got_s[i], want_s[i], f"{what} tensor {i}", block_size)
         exact.append(exact_fraction(mode, [got_p[i], *got_s[i]], [want_p[i], *want_s[i]]))
     return min(exact)
 
@@ -120,6 +120,62 @@ def test_q8_step_ragged_list(psa, case, grad_dtype, mode):
                                             grad_kind="student_t_outliers", grad_std=1e-3)
     ex = check_all(mode, got_p, want_p, got_s, want_s, f"{mode}/{case}/{grad_dtype}")
     assert ex == 1.0, f"expected bit-identical results, exact fraction {ex}"
+
+
+# ------------------------------------------------------------------ any block size, any percentile
+# (the general kernel: one CTA per block, shared-memory staging, radix-select ranks)
+ANY_CASES = {
+    "bs1_rne": (Q8Opts(False, 42, 100.0, block_size=1), [1, 2, 33, 300]),
+    "bs3_sr": (Q8Opts(True, 42, 100.0, block_size=3), [1, 2, 7, 1000]),
+    "bs64_rne": (Q8Opts(False, 42, 100.0, block_size=64), [1, 63, 64, 65, 5000]),
+    "bs100_sr_p99": (Q8Opts(True, 9, 99.0, block_size=100), [1, 99, 100, 101, 7777]),
+    "bs256_static": (Q8Opts(False, 42, 100.0, True, block_size=256), [5, 256, 70001]),
+    "bs1000_p90": (Q8Opts(False, 42, 90.0, block_size=1000), [17, 999, 1000, 1001, 12345]),
+    "bs4096_sr_p99.9": (Q8Opts(True, 3, 99.9, block_size=4096), [1, 4095, 4097, 20000]),
+    "bs16384_rne": (Q8Opts(False, 42, 100.0, block_size=16384), [1, 16383, 16385, 40000]),
+    "bs2048_p90": (Q8Opts(False, 42, 90.0), RAGGED),            # rank 205: general kernel at 2048
+    "bs2048_sr_p50": (Q8Opts(True, 11, 50.0), [1, 2047, 2049, 9000]),
+    "bs2048_p99_static": (Q8Opts(False, 42, 99.0, True), [3000, 2048]),
+}
+
+
+@pytest.mark.parametrize("mode", ["q8", "q8v"])
+@pytest.mark.parametrize("case", sorted(ANY_CASES))
+def test_q8_any_block_size_and_rank(psa, case, mode):
+    q8, sizes = ANY_CASES[case]
+    hp = HParams(lr=1e-3, weight_decay=0.1)
+    gd = "bf16" if case.endswith("sr") else "f32"
+    got_p, want_p, got_s, want_s = run_both(psa, mode, sizes, 4, hp, q8, grad_dtype=gd,
+                                            grad_kind="student_t_outliers", grad_std=1e-3)
+    ex = check_all(mode, got_p, want_p, got_s, want_s, f"{mode}/{case}", q8.block_size)
+    assert ex == 1.0, f"expected bit-identical results, exact fraction {ex}"
+
+
+@pytest.mark.parametrize("case", ["bs1_rne", "bs100_sr_p99", "bs1000_p90", "bs16384_rne", "bs2048_sr_p50"])
+def test_quantize_dequantize_any_block_size(psa, case):
+    q8, sizes = ANY_CASES[case]
+    bs = q8.block_size
+    ms, vs = [], []
+    for i, n in enumerate(sizes):
+        m, v = workloads.random_moments_np(n, seed=40 + i)
+        ms.append(m)
+        vs.append(v)
+    dm, dv = _to_dev(ms), _to_dev(vs)
+    mc, vc, msc, vsc = psa.zeros_state(dm, "q8", bs)
+    psa.q8_quantize(dm, dv, mc, vc, msc, vsc, step=4, **q8_kwargs(q8, step=False))
+    back_m = [torch.empty_like(x) for x in dm]
+    back_v = [torch.empty_like(x) for x in dv]
+    psa.q8_dequantize(mc, vc, msc, vsc, back_m, back_v, block_size=bs)
+    torch.cuda.synchronize()
+    for i in range(len(sizes)):
+        want = oracle.quantize(ms[i], vs[i], q8, step=4, tensor_idx=i)
+        got = (mc[i].cpu().numpy(), vc[i].cpu().numpy(), msc[i].cpu().numpy(), vsc[i].cpu().numpy())
+        for g, w, name in zip(got, want, ("m codes", "v codes", "m scales", "v scales")):
+            np.testing.assert_array_equal(np.ascontiguousarray(g).view(np.uint8), np.ascontiguousarray(w).view(np.uint8),
+                                          err_msg=f"{case} tensor {i} {name}")
+        wm, wv = oracle.dequantize(*want, block_size=bs)
+        np.testing.assert_array_equal(back_m[i].cpu().numpy().view(np.uint32), wm.view(np.uint32))
+        np.testing.assert_array_equal(back_v[i].cpu().numpy().view(np.uint32), wv.view(np.uint32))
 
 
 def test_zero_grads_are_pure_decay(psa):

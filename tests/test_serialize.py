@@ -66,3 +66,29 @@ def test_damaged_and_mismatched_files_are_rejected(psa):
     with pytest.raises(ValueError):
         bad = (st[0], st[1], st[2], [torch.zeros(5)])  # wrong scale count
         psa.save_state(io.BytesIO(), "q8", bad, step=1)
+
+
+@pytest.mark.parametrize("mode", ["q8", "q8v"])
+def test_round_trip_other_block_size(psa, mode):
+    sizes = [1, 300, 1000]
+    bs = 256
+    g = torch.Generator().manual_seed(5)
+    nb = lambda n: (n + bs - 1) // bs
+    if mode == "q8":
+        st = ([torch.randint(-127, 128, (n,), generator=g, dtype=torch.int8) for n in sizes],
+              [torch.randint(0, 256, (n,), generator=g, dtype=torch.uint8) for n in sizes],
+              [torch.rand(nb(n), generator=g) for n in sizes], [torch.rand(nb(n), generator=g) for n in sizes])
+    else:
+        st = ([torch.randn(n, generator=g) for n in sizes],
+              [torch.randint(0, 256, (n,), generator=g, dtype=torch.uint8) for n in sizes],
+              [torch.rand(nb(n), generator=g) for n in sizes])
+    buf = io.BytesIO()
+    psa.save_state(buf, mode, st, step=3, block_size=bs)
+    buf.seek(0)
+    mode2, st2, step, header = psa.load_state(buf)
+    assert header["block_size"] == bs and mode2 == mode and step == 3
+    for a_part, b_part in zip(st, st2):
+        for a, b in zip(a_part, b_part):
+            assert torch.equal(a, b)
+    with pytest.raises(ValueError):  # scales sized for the default block
+        psa.save_state(io.BytesIO(), mode, st, step=3)
