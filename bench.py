@@ -3,6 +3,10 @@
 python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                 [--workload flat_16m] [--modes q8,bf16m,fp32] [--no-cpu-baseline]
 
+A mode is fp32, bf16m, q8 or q8v, optionally with 8-bit overrides: "q8/bs256" (block size
+256), "q8/p99" (percentile 99), "q8v/bs4096/p99.9". Overrides away from block 2048 or to a
+percentile rank above 16 run the library's general kernel.
+
 One step = one call of the library over the workload's whole tensor list (load, dequantize,
 AdamW, requantize, store: a single kernel launch per <=440 tensors). The headline workload
 is the 8-bit block-wise AdamW step on one fp32 tensor of 16,777,216 params (block 2048,
@@ -43,7 +47,23 @@ L2_FLUSH_BYTES = 384 << 20
 STATE_BYTES = {"fp32": (4, 4), "bf16m": (2, 2), "q8": (1, 1), "q8v": (4, 1)}   # per m, v element
 
 
-def algorithmic_bytes(mode: str, sizes, grad_dtype: str, zero_grads: bool = False) -> int:
+def parse_mode(spec: str):
+    """"q8/bs256/p99" -> ("q8", {"block_size": 256, "percentile": 99.0})."""
+    base, *opts = spec.split("/")
+    if base not in STATE_BYTES:
+        raise SystemExit(f"unknown moment mode {base!r}")
+    over = {}
+    for o in opts:
+        if o.startswith("bs") and base in ("q8", "q8v"):
+            over["block_size"] = int(o[2:])
+        elif o.startswith("p") and base in ("q8", "q8v"):
+            over["percentile"] = float(o[1:])
+        else:
+            raise SystemExit(f"bad mode option {o!r} in {spec!r}")
+    return base, over
+
+
+def algorithmic_bytes(mode: str, sizes, grad_dtype: str, zero_grads: bool = False, block_size: int = 2048) -> int:
     """Bytes the step must move once each: p read+write, g read (and written with zeros
     when zero_grads), m and v read+write, and for 8-bit moments the fp32 scales of every
     block read+write."""
@@ -52,7 +72,7 @@ def algorithmic_bytes(mode: str, sizes, grad_dtype: str, zero_grads: bool = Fals
     per = 8 + g * (2 if zero_grads else 1) + 2 * mb + 2 * vb
     total = per * sum(sizes)
     scales = {"q8": 2, "q8v": 1}.get(mode, 0)  # fp32 scale arrays, read + written per block
-    total += 8 * scales * sum((n + 2047) // 2048 for n in sizes)
+    total += 8 * scales * sum((n + block_size - 1) // block_size for n in sizes)
     return total
 
 
@@ -182,12 +202,15 @@ def run_ours(args, rank: int, world: int, dist):
     clocks.start()
     results = {}
     modes = args.modes
-    for mode in modes:
+    for spec in modes:
+        mode, over = parse_mode(spec)
+        bs = over.get("block_size", 2048)
         params = workloads.init_params_torch(w.specs, dev, seed=workloads.DEFAULT_SEED + rank)
-        state = psa.zeros_state(params, mode)
+        state = psa.zeros_state(params, mode, bs)
         kw = dict(lr=w.lr, beta1=w.beta1, beta2=w.beta2, eps=w.eps, weight_decay=w.weight_decay)
         if mode in ("q8", "q8v"):
             kw.update(stochastic_rounding=w.stochastic_rounding, seed=w.seed, percentile=w.percentile)
+            kw.update(over)
         if args.zero_grads:
             kw.update(zero_grads=True)
         launches_per_step = -(-len([n for n in sizes if n > 0]) // (8 if len(sizes) <= 8 else 440))
@@ -222,9 +245,9 @@ def run_ours(args, rank: int, world: int, dist):
             dist.barrier()
         step_ms = [a.elapsed_time(b) for a, b in evs]
         total_s = max_over_ranks(sum(step_ms) / 1e3, dist, dev)
-        nbytes = algorithmic_bytes(mode, sizes, w.grad_dtype, args.zero_grads)
+        nbytes = algorithmic_bytes(mode, sizes, w.grad_dtype, args.zero_grads, bs)
         mean_s = sum(step_ms) / len(step_ms) / 1e3
-        results[mode] = {
+        results[spec] = {
             "gparams_per_s": job_gparams_per_s(numel, args.steps, total_s, world),
             "ms_per_step": total_s * 1e3 / args.steps,
             "median_ms": statistics.median(step_ms),
@@ -233,9 +256,9 @@ def run_ours(args, rank: int, world: int, dist):
             "launches": launches_per_step * args.steps,
         }
         # ---- end to end through the public API with host buffers
-        if mode == args.modes[0]:
-            results[mode]["e2e"] = run_e2e(args, psa, torch, dev, stream, w, params, state, kw, t, flush, dist, world)
-            results[mode]["launches"] += launches_per_step * args.steps
+        if spec == args.modes[0]:
+            results[spec]["e2e"] = run_e2e(args, psa, torch, dev, stream, w, params, state, kw, t, flush, dist, world)
+            results[spec]["launches"] += launches_per_step * args.steps
         del plans, params, state
         torch.cuda.empty_cache()
     clk = clocks.stop()
@@ -249,7 +272,7 @@ def run_e2e(args, psa, torch, dev, stream, w, params, state, kw, t, flush, dist,
     host_g = [[g.cpu().pin_memory() for g in gs] for gs in host_g]
     host_p = [torch.empty(p.numel(), dtype=torch.float32, pin_memory=True) for p in params]
     dev_g = [torch.empty(n, dtype=gdt, device=dev) for n in sizes]
-    plan = psa.StepPlan(args.modes[0], params, dev_g, state, **kw)
+    plan = psa.StepPlan(parse_mode(args.modes[0])[0], params, dev_g, state, **kw)
     h2d = sum(g.numel() * g.element_size() for g in host_g[0])
     d2h = sum(p.numel() * 4 for p in params)
     for i in range(3):  # warm the copy engines
@@ -283,12 +306,14 @@ def run_e2e(args, psa, torch, dev, stream, w, params, state, kw, t, flush, dist,
 
 
 # ------------------------------------------------------------------ the CPU oracle as a baseline
-def oracle_sample_rate(w: workloads.Workload, mode: str, budget_s: float):
+def oracle_sample_rate(w: workloads.Workload, spec: str, budget_s: float):
     """Time the CPU oracle (as it is: plain scalar C, one thread) on whole 2048-element
     blocks of the workload's first tensor, step after step, for about `budget_s` seconds."""
     import numpy as np
     import oracle
 
+    mode, over = parse_mode(spec)
+    bs = over.get("block_size", 2048)
     n = min(w.sizes[0], 256 * 2048)
     rng = np.random.default_rng(0)
     p = (rng.standard_normal(n) * 0.02).astype(np.float32)
@@ -297,15 +322,15 @@ def oracle_sample_rate(w: workloads.Workload, mode: str, budget_s: float):
     elif mode == "bf16m":
         st = [np.zeros(n, np.uint16), np.zeros(n, np.uint16)]
     elif mode == "q8v":
-        st = [np.zeros(n, np.float32), np.zeros(n, np.uint8), np.zeros(oracle.n_blocks(n), np.float32)]
+        st = [np.zeros(n, np.float32), np.zeros(n, np.uint8), np.zeros(oracle.n_blocks(n, bs), np.float32)]
     else:
-        nb = oracle.n_blocks(n)
+        nb = oracle.n_blocks(n, bs)
         st = [np.zeros(n, np.int8), np.zeros(n, np.uint8), np.zeros(nb, np.float32), np.zeros(nb, np.float32)]
     g = (rng.standard_normal(n) * w.grad_std).astype(np.float32)
     if w.grad_dtype == "bf16":
         g = (g.view(np.uint32) >> 16).astype(np.uint16)
     hp = oracle.HParams(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay)
-    q8 = oracle.Q8Opts(w.stochastic_rounding, w.seed, w.percentile)
+    q8 = oracle.Q8Opts(w.stochastic_rounding, w.seed, over.get("percentile", w.percentile), block_size=bs)
     done, t, t0 = 0, 0, time.perf_counter()
     while True:
         t += 1
@@ -314,7 +339,7 @@ def oracle_sample_rate(w: workloads.Workload, mode: str, budget_s: float):
         el = time.perf_counter() - t0
         if el >= budget_s:
             break
-    return done / el / 1e9, f"{t} steps over the first {n:,} params of the workload ({n // 2048} blocks), " \
+    return done / el / 1e9, f"{t} steps over the first {n:,} params of the workload ({-(-n // bs)} blocks), " \
                             f"{el:.1f} s, one thread"
 
 
@@ -373,7 +398,8 @@ def main():
         args.workload = w.name
     if args.modes is None:
         rest = [m for m in ("q8", "bf16m", "fp32", "q8v") if m != w.mode]
-        args.modes = [w.mode] + rest
+        # the general kernel: another block size, and a percentile rank above 16
+        args.modes = [w.mode] + rest + ["q8/bs256", "q8/p99"]
     else:
         args.modes = args.modes.split(",")
     if args.warmup < 3:
