@@ -87,10 +87,10 @@ typedef struct {
 } psadam_hparams;
 
 /* 8-bit options (PR #814's BlockSize, UseStochasticRounding, QuantizationPercentile).
- * Speed: block_size 2048 with a rank k <= 16 (percentile >= ~99.27, 100 included) runs the
- * specialised 2048-block kernels; any other block size or a lower percentile runs a general
- * kernel (one CTA per block, shared-memory staging, radix select) with identical results
- * for identical inputs, only slower. */
+ * Speed: block_size 2048 with a rank k <= 4 (percentile >= 99.81 on full blocks; 100 and
+ * the default 99.9 included) runs the specialised 2048-block kernels; any other block size
+ * or a lower percentile runs a general kernel (tiles of whole blocks, shared-memory
+ * staging, radix select) with identical results for identical inputs, only slower. */
 typedef struct {
     int32_t block_size;          /* elements per block, 1..16384 (INVALID_ARG below 1,
                                     UNSUPPORTED above); PR #814's default is 2048 */

@@ -131,9 +131,12 @@ struct GradSide {
 };
 
 // Pack the list into as few launches as fit and run `fn` on each.
+// bs: quantization block; unit: elements per CTA (bs for the 2048-block kernels, a tile of
+// whole blocks for the general ones).
 template <int CAP, typename Fn>
 int run_launches(const std::vector<Entry>& es, const StepConsts& c, uint64_t seed, int64_t step, float pct,
-                 const GradSide& gs, Fn fn, cudaStream_t stream, int bs = kBlock) {
+                 const GradSide& gs, Fn fn, cudaStream_t stream, int bs = kBlock, int unit = 0) {
+  if (unit == 0) unit = bs;
   static thread_local LaunchArgs<CAP> a;  // ~32 KB: keep it off the stack
   std::memset(&a, 0, sizeof a);
   a.c = c;
@@ -145,13 +148,14 @@ int run_launches(const std::vector<Entry>& es, const StepConsts& c, uint64_t see
   a.seed_hi = (uint32_t)(seed >> 32);
   a.step_lo = (uint32_t)step;
   a.block_size = bs;
+  a.tile = unit;
   a.k_full = percentile_rank(pct, bs);
   size_t i = 0;
   while (i < es.size()) {
     int nt = 0;
     long long blocks = 0;
     while (i < es.size() && nt < CAP) {
-      const long long nb = n_blocks(es[i].numel, bs);
+      const long long nb = n_blocks(es[i].numel, unit);
       if (blocks + nb > INT_MAX) break;
       TensorRef& t = a.t[nt++];
       t.p = es[i].p;
@@ -186,8 +190,7 @@ Launcher<CAP> pick_step(int mode, bool gb, bool sr, int K) {
   if (mode == kModeBF16) return gb ? PSADAM_STEP_FN(kModeBF16, true, false, 1, CAP) : PSADAM_STEP_FN(kModeBF16, false, false, 1, CAP);
 #define PSADAM_PICK_K(MODE, GB, SR)                                 \
   if (K == 1) return PSADAM_STEP_FN(MODE, GB, SR, 1, CAP);          \
-  if (K == 4) return PSADAM_STEP_FN(MODE, GB, SR, 4, CAP);          \
-  return PSADAM_STEP_FN(MODE, GB, SR, 16, CAP);
+  return PSADAM_STEP_FN(MODE, GB, SR, 4, CAP);
 #define PSADAM_PICK_MODE(MODE)                                      \
   if (gb) {                                                         \
     if (sr) { PSADAM_PICK_K(MODE, true, true) } else { PSADAM_PICK_K(MODE, true, false) } \
@@ -212,18 +215,22 @@ Launcher<CAP> pick_step_any(int mode, bool gb, bool sr) {
 
 template <int CAP>
 Launcher<CAP> pick_quantize(bool sr, int K) {
-  if (sr) return K == 1 ? &launch_quantize<true, 1, CAP> : (K == 4 ? &launch_quantize<true, 4, CAP> : &launch_quantize<true, 16, CAP>);
-  return K == 1 ? &launch_quantize<false, 1, CAP> : (K == 4 ? &launch_quantize<false, 4, CAP> : &launch_quantize<false, 16, CAP>);
+  if (sr) return K == 1 ? &launch_quantize<true, 1, CAP> : &launch_quantize<true, 4, CAP>;
+  return K == 1 ? &launch_quantize<false, 1, CAP> : &launch_quantize<false, 4, CAP>;
 }
 
 // Dispatch on list length: short lists use the small parameter block.
 int dispatch(const std::vector<Entry>& es, const StepConsts& c, uint64_t seed, int64_t step, float pct,
              Launcher<kCapSmall> small, Launcher<kCapLarge> large, cudaStream_t stream,
-             const GradSide& gs = GradSide{}, int bs = kBlock) {
+             const GradSide& gs = GradSide{}, int bs = kBlock, int unit = 0) {
   if (es.empty()) return PSADAM_OK;
-  if (es.size() <= (size_t)kCapSmall) return run_launches<kCapSmall>(es, c, seed, step, pct, gs, small, stream, bs);
-  return run_launches<kCapLarge>(es, c, seed, step, pct, gs, large, stream, bs);
+  if (es.size() <= (size_t)kCapSmall)
+    return run_launches<kCapSmall>(es, c, seed, step, pct, gs, small, stream, bs, unit);
+  return run_launches<kCapLarge>(es, c, seed, step, pct, gs, large, stream, bs, unit);
 }
+
+// Elements per CTA of the general kernels for block size bs.
+int any_tile(int bs) { return any_blocks_per_tile(bs) * bs; }
 
 // The list's grad-side options; 0 as an unscale factor reads as 1 (a zeroed struct changes nothing).
 int grad_side(const psadam_list* list, GradSide& gs) {
@@ -285,7 +292,7 @@ int step_common(int mode, const psadam_list* list, const void* const* m, const v
   // 2048-element blocks with rank <= 16: the specialised kernels; otherwise one CTA per block
   if (q8mode && (bs != kBlock || kmax > kMaxRank))
     return dispatch(es, c, seed, step, pct, pick_step_any<kCapSmall>(mode, gb, sr), pick_step_any<kCapLarge>(mode, gb, sr),
-                    s, gs, bs);
+                    s, gs, bs, any_tile(bs));
   const int K = rank_template(kmax);
   return dispatch(es, c, seed, step, pct, pick_step<kCapSmall>(mode, gb, sr, K), pick_step<kCapLarge>(mode, gb, sr, K),
                   s, gs);
@@ -346,7 +353,7 @@ int psadam_q8_quantize(int32_t n_tensors, const int64_t* numel, const float* con
     return dispatch(es, StepConsts{}, q8->seed, step, q8->percentile,
                     sr ? &launch_quantize_any<true, kCapSmall> : &launch_quantize_any<false, kCapSmall>,
                     sr ? &launch_quantize_any<true, kCapLarge> : &launch_quantize_any<false, kCapLarge>, s, GradSide{},
-                    bs);
+                    bs, any_tile(bs));
   const int K = rank_template(kmax);
   return dispatch(es, StepConsts{}, q8->seed, step, q8->percentile, pick_quantize<kCapSmall>(sr, K),
                   pick_quantize<kCapLarge>(sr, K), s);
@@ -372,7 +379,7 @@ int psadam_q8_dequantize(int32_t n_tensors, const int64_t* numel, const int8_t* 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (block_size != kBlock)
     return dispatch(es, StepConsts{}, 0, 1, 100.f, &launch_dequantize_any<kCapSmall>, &launch_dequantize_any<kCapLarge>,
-                    s, GradSide{}, block_size);
+                    s, GradSide{}, block_size, any_tile(block_size));
   return dispatch(es, StepConsts{}, 0, 1, 100.f, &launch_dequantize<kCapSmall>, &launch_dequantize<kCapLarge>, s);
 }
 

@@ -17,10 +17,19 @@ constexpr int kWarps = kThreads / 32;
 // long lists the largest block that stays under the 32,764-byte parameter limit.
 constexpr int kCapSmall = 8;
 constexpr int kCapLarge = 440;
-constexpr int kMaxRank = 16;  // largest percentile rank k the 2048-block kernels select
+// Largest percentile rank k the 2048-block kernels select (their top-K merge network; for
+// higher ranks the general kernel's radix select measured faster).
+constexpr int kMaxRank = 4;
 // Largest quantization block of the any-block-size kernels (its fp32 m', v' are staged in
 // shared memory: 128 KB for both moments).
 constexpr int kMaxAnyBlock = 16384;
+// The general kernels' CTA takes a tile of whole blocks: as many as fit 2048 elements, at
+// most kAnyMaxQ of them (one block when B > 2048).
+constexpr int kAnyMaxQ = 64;
+constexpr int kAnyTile = 2048;
+constexpr int any_blocks_per_tile(int B) {
+  return B >= kAnyTile ? 1 : (kAnyTile / B < kAnyMaxQ ? kAnyTile / B : kAnyMaxQ);
+}
 
 enum Mode : int { kModeF32 = 0, kModeBF16 = 1, kModeQ8 = 2, kModeQ8V = 3 };  // Q8V: fp32 m, 8-bit v
 
@@ -58,12 +67,14 @@ struct LaunchArgs {
   const int* skip;  // device flag or null: a nonzero value makes the launch a no-op
   int static_scales;  // 8-bit: a block's nonzero scale is kept instead of recomputed
   int block_size;     // 8-bit quantization block (the 2048-block kernels assume 2048)
+  int tile;           // elements per CTA (a whole number of blocks)
+  int pad_;
   TensorRef t[CAP];
 };
 static_assert(sizeof(LaunchArgs<kCapLarge>) <= 32764, "kernel parameter block too large");
 
-// Rank templates: K = 1 (absmax), 4 or 16 (k-th largest for k <= K).
-constexpr int rank_template(int k) { return k <= 1 ? 1 : (k <= 4 ? 4 : 16); }
+// Rank templates: K = 1 (absmax) or 4 (k-th largest for k <= 4).
+constexpr int rank_template(int k) { return k <= 1 ? 1 : 4; }
 
 // Launchers, explicitly instantiated in the kernel translation units.
 template <int MODE, bool GBF16, bool SR, int K, int CAP>

@@ -105,7 +105,7 @@ Q8_CASES = {
     "sr_absmax": Q8Opts(True, 42, 100.0),
     "rne_p99.9": Q8Opts(False, 42, 99.9),   # rank 3 of a full block (K = 4 kernel)
     "sr_p99.9": Q8Opts(True, 7, 99.9),
-    "rne_p99.5": Q8Opts(False, 42, 99.5),   # rank 11 (K = 16 kernel)
+    "rne_p99.5": Q8Opts(False, 42, 99.5),   # rank 11: the general kernel's radix select
     "rne_static": Q8Opts(False, 42, 100.0, True),  # scales kept after the first step
     "sr_static_p99.9": Q8Opts(True, 5, 99.9, True),
 }
