@@ -380,7 +380,9 @@ def test_flat_16m_q8_full(psa):
 
 
 def _sample_blocks(nb: int):
-    return sorted({0, nb - 1, *range(0, nb, 257)})
+    # block 0, the last, every 257th, and the blocks on either side of element 2^31
+    edge = {b for b in ((2 ** 31 - 1) // 2048, 2 ** 31 // 2048) if b < nb}
+    return sorted({0, nb - 1, *range(0, nb, 257), *edge})
 
 
 def sampled_run(psa, w: workloads.Workload, mode: str, steps: int, tensor_stride: int = 1):
@@ -452,6 +454,18 @@ def sampled_run(psa, w: workloads.Workload, mode: str, steps: int, tensor_stride
         exact = min(exact, exact_fraction(mode, [got_p, *got_s], [p, *st]))
     del params, state, gbuf
     return exact, len(picks)
+
+
+@pytest.mark.parametrize("mode", ["q8", "fp32"])
+def test_tensor_past_2_31_elements_sampled(psa, mode):
+    """One tensor of 2^31 + 2049 elements: element offsets beyond the 32-bit range, blocks
+    on both sides of element 2^31 checked against the oracle (8-bit with stochastic
+    rounding and percentile 99.9, and fp32 moments)."""
+    n = 2 ** 31 + 2049
+    w = workloads.Workload("flat_2g_edge", (workloads.TensorSpec("w", (n,)),), "q8", grad_std=1e-3,
+                           weight_decay=0.01, steps=2, stochastic_rounding=True, percentile=99.9)
+    ex, picks = sampled_run(psa, w, mode, 2)
+    assert picks > 4000 and ex == 1.0
 
 
 def test_vit_base_list_sampled(psa):
