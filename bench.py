@@ -3,9 +3,10 @@
 python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                 [--workload flat_16m] [--modes q8,bf16m,fp32] [--no-cpu-baseline]
 
-A mode is fp32, bf16m, q8 or q8v, optionally with 8-bit overrides: "q8/bs256" (block size
-256), "q8/p99" (percentile 99), "q8v/bs4096/p99.9". Overrides away from block 2048 or to a
-percentile rank above 16 run the library's general kernel.
+A mode is fp32, bf16m, q8 or q8v, optionally with overrides: "q8/bs256" (block size 256),
+"q8/p99" (percentile 99), "q8v/bs4096/p99.9", and "/approx" for the opt-in approximate
+square root and quotient in the update (any mode). Overrides away from block 2048 or to a
+percentile rank above 4 run the library's general kernel.
 
 One step = one call of the library over the workload's whole tensor list (load, dequantize,
 AdamW, requantize, store: a single kernel launch per <=440 tensors). The headline workload
@@ -54,7 +55,9 @@ def parse_mode(spec: str):
         raise SystemExit(f"unknown moment mode {base!r}")
     over = {}
     for o in opts:
-        if o.startswith("bs") and base in ("q8", "q8v"):
+        if o == "approx":
+            over["approx_update"] = True
+        elif o.startswith("bs") and base in ("q8", "q8v"):
             over["block_size"] = int(o[2:])
         elif o.startswith("p") and base in ("q8", "q8v"):
             over["percentile"] = float(o[1:])
@@ -210,7 +213,7 @@ def run_ours(args, rank: int, world: int, dist):
         kw = dict(lr=w.lr, beta1=w.beta1, beta2=w.beta2, eps=w.eps, weight_decay=w.weight_decay)
         if mode in ("q8", "q8v"):
             kw.update(stochastic_rounding=w.stochastic_rounding, seed=w.seed, percentile=w.percentile)
-            kw.update(over)
+        kw.update(over)
         if args.zero_grads:
             kw.update(zero_grads=True)
         launches_per_step = -(-len([n for n in sizes if n > 0]) // (8 if len(sizes) <= 8 else 440))
@@ -398,8 +401,9 @@ def main():
         args.workload = w.name
     if args.modes is None:
         rest = [m for m in ("q8", "bf16m", "fp32", "q8v") if m != w.mode]
-        # the general kernel: another block size, and a percentile rank above 16
-        args.modes = [w.mode] + rest + ["q8/bs256", "q8/p99"]
+        # the opt-in approximate update; the general kernel: another block size, and a
+        # percentile rank above 4
+        args.modes = [w.mode] + rest + ["q8/approx", "q8/bs256", "q8/p99"]
     else:
         args.modes = args.modes.split(",")
     if args.warmup < 3:

@@ -52,7 +52,7 @@ class _List(ctypes.Structure):
     _fields_ = [("n_tensors", ctypes.c_int32), ("grad_dtype", ctypes.c_int32),
                 ("numel", ctypes.POINTER(ctypes.c_int64)), ("param", ctypes.POINTER(ctypes.c_void_p)),
                 ("grad", ctypes.POINTER(ctypes.c_void_p)), ("grad_unscale", ctypes.c_float),
-                ("zero_grads", ctypes.c_int32), ("skip_if_set", ctypes.c_void_p)]
+                ("zero_grads", ctypes.c_int32), ("skip_if_set", ctypes.c_void_p), ("approx_update", ctypes.c_int32)]
 
 
 _lib = ctypes.CDLL(LIB_PATH)
@@ -157,7 +157,8 @@ def _skip_ptr(skip_flag) -> int | None:
     return skip_flag.data_ptr()
 
 
-def _list(params, grads, grad_unscale: float = 1.0, zero_grads: bool = False, skip_flag=None, like=None):
+def _list(params, grads, grad_unscale: float = 1.0, zero_grads: bool = False, skip_flag=None, like=None,
+          approx_update: bool = False):
     if like is None:
         like = params
         if len(params) != len(grads):
@@ -170,7 +171,7 @@ def _list(params, grads, grad_unscale: float = 1.0, zero_grads: bool = False, sk
     keep = (_numels(like), _ptrs(params) if params is not None else None, _ptrs(grads))
     lst = _List(len(grads), GRAD_BF16 if gdt == torch.bfloat16 else GRAD_F32, keep[0],
                 ctypes.cast(keep[1], _PP) if keep[1] is not None else None, ctypes.cast(keep[2], _PP),
-                grad_unscale, int(bool(zero_grads)), _skip_ptr(skip_flag))
+                grad_unscale, int(bool(zero_grads)), _skip_ptr(skip_flag), int(bool(approx_update)))
     return lst, keep
 
 
@@ -182,12 +183,15 @@ def _raise(status: int, where: str) -> None:
 # ------------------------------------------------------------------ steps
 def adam_step_fp32(params, grads, m, v, step: int, lr: float = 1e-3, beta1: float = 0.9, beta2: float = 0.999,
                    eps: float = 1e-8, weight_decay: float = 0.0, grad_unscale: float = 1.0, zero_grads: bool = False,
-                   skip_flag=None, stream=None) -> None:
+                   skip_flag=None, approx_update: bool = False, stream=None) -> None:
     """One AdamW step with fp32 moments, in place, enqueued on ``stream`` (default: current).
     Grad side: grads are multiplied by ``grad_unscale`` before use, overwritten with zeros
     after use when ``zero_grads``, and the whole step is skipped on the device when the
-    CUDA int32 tensor ``skip_flag`` holds a nonzero value (see :func:`check_grads`)."""
-    lst, keep = _list(params, grads, grad_unscale, zero_grads, skip_flag)
+    CUDA int32 tensor ``skip_flag`` holds a nonzero value (see :func:`check_grads`).
+    ``approx_update`` opts into the hardware's approximate square root and quotient in the
+    parameter update (about 10 % faster for 8-bit moments; params within a few ulp of the
+    update of the IEEE result, every moment, code and scale still exact)."""
+    lst, keep = _list(params, grads, grad_unscale, zero_grads, skip_flag, approx_update=approx_update)
     _check_layout("m", m, torch.float32, params)
     _check_layout("v", v, torch.float32, params)
     mp, vp = _ptrs(m), _ptrs(v)
@@ -198,10 +202,10 @@ def adam_step_fp32(params, grads, m, v, step: int, lr: float = 1e-3, beta1: floa
 
 def adam_step_bf16m(params, grads, m, v, step: int, lr: float = 1e-3, beta1: float = 0.9, beta2: float = 0.999,
                    eps: float = 1e-8, weight_decay: float = 0.0, grad_unscale: float = 1.0, zero_grads: bool = False,
-                   skip_flag=None, stream=None) -> None:
+                   skip_flag=None, approx_update: bool = False, stream=None) -> None:
     """One AdamW step with bf16 moments (torch.bfloat16 tensors), in place (grad-side
     options as for :func:`adam_step_fp32`)."""
-    lst, keep = _list(params, grads, grad_unscale, zero_grads, skip_flag)
+    lst, keep = _list(params, grads, grad_unscale, zero_grads, skip_flag, approx_update=approx_update)
     _check_layout("m", m, torch.bfloat16, params)
     _check_layout("v", v, torch.bfloat16, params)
     mp, vp = _ptrs(m), _ptrs(v)
@@ -218,10 +222,11 @@ def _q8(stochastic_rounding: bool, seed: int, percentile: float, block_size: int
 def adam_step_q8(params, grads, m_code, v_code, m_scale, v_scale, step: int, lr: float = 1e-3, beta1: float = 0.9,
                  beta2: float = 0.999, eps: float = 1e-8, weight_decay: float = 0.0, stochastic_rounding: bool = False,
                  seed: int = 42, percentile: float = 100.0, block_size: int = BLOCK, grad_unscale: float = 1.0,
-                 zero_grads: bool = False, skip_flag=None, static_scales: bool = False, stream=None) -> None:
+                 zero_grads: bool = False, skip_flag=None, static_scales: bool = False, approx_update: bool = False,
+                 stream=None) -> None:
     """One AdamW step with 8-bit block-wise moments (int8 m codes, uint8 v codes, fp32
     per-block scales), dequantize-update-requantize in one pass, in place."""
-    lst, keep = _list(params, grads, grad_unscale, zero_grads, skip_flag)
+    lst, keep = _list(params, grads, grad_unscale, zero_grads, skip_flag, approx_update=approx_update)
     _check_layout("m_code", m_code, torch.int8, params)
     _check_layout("v_code", v_code, torch.uint8, params)
     _check_layout("m_scale", m_scale, torch.float32, params, _nb(block_size))
@@ -237,10 +242,11 @@ def adam_step_q8(params, grads, m_code, v_code, m_scale, v_scale, step: int, lr:
 def adam_step_q8v(params, grads, m, v_code, v_scale, step: int, lr: float = 1e-3, beta1: float = 0.9,
                   beta2: float = 0.999, eps: float = 1e-8, weight_decay: float = 0.0, stochastic_rounding: bool = False,
                   seed: int = 42, percentile: float = 100.0, block_size: int = BLOCK, grad_unscale: float = 1.0,
-                  zero_grads: bool = False, skip_flag=None, static_scales: bool = False, stream=None) -> None:
+                  zero_grads: bool = False, skip_flag=None, static_scales: bool = False, approx_update: bool = False,
+                 stream=None) -> None:
     """One AdamW step with an fp32 first moment and an 8-bit block-wise second moment
     (uint8 v codes, fp32 per-block scales), in place."""
-    lst, keep = _list(params, grads, grad_unscale, zero_grads, skip_flag)
+    lst, keep = _list(params, grads, grad_unscale, zero_grads, skip_flag, approx_update=approx_update)
     _check_layout("m", m, torch.float32, params)
     _check_layout("v_code", v_code, torch.uint8, params)
     _check_layout("v_scale", v_scale, torch.float32, params, _nb(block_size))
@@ -341,12 +347,12 @@ class StepPlan:
                  beta2: float = 0.999, eps: float = 1e-8, weight_decay: float = 0.0,
                  stochastic_rounding: bool = False, seed: int = 42, percentile: float = 100.0,
                  block_size: int = BLOCK, grad_unscale: float = 1.0, zero_grads: bool = False, skip_flag=None,
-                 static_scales: bool = False):
+                 static_scales: bool = False, approx_update: bool = False):
         if mode not in MODES:
             raise ValueError(f"unknown moment mode {mode!r}")
         self.mode = mode
         self._skip = skip_flag
-        self._lst, self._keep = _list(params, grads, grad_unscale, zero_grads, skip_flag)
+        self._lst, self._keep = _list(params, grads, grad_unscale, zero_grads, skip_flag, approx_update=approx_update)
         self._grad_dtype = grads[0].dtype if grads else torch.float32
         self._params = list(params)
         if mode == "fp32":

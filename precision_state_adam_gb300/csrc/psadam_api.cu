@@ -128,6 +128,7 @@ struct GradSide {
   int zero = 0;
   const int* skip = nullptr;
   int static_scales = 0;  // not grad-side, but carried the same way into the launch
+  int approx = 0;         // likewise: approximate square root and division in the update
 };
 
 // Pack the list into as few launches as fit and run `fn` on each.
@@ -144,6 +145,7 @@ int run_launches(const std::vector<Entry>& es, const StepConsts& c, uint64_t see
   a.zero_grads = gs.zero;
   a.skip = gs.skip;
   a.static_scales = gs.static_scales;
+  a.approx = gs.approx;
   a.seed_lo = (uint32_t)(seed & 0xFFFFFFFFu);
   a.seed_hi = (uint32_t)(seed >> 32);
   a.step_lo = (uint32_t)step;
@@ -238,6 +240,7 @@ int grad_side(const psadam_list* list, GradSide& gs) {
   if (!finite(gs.unscale)) return PSADAM_ERR_INVALID_ARG;
   gs.zero = list->zero_grads != 0;
   gs.skip = list->skip_if_set;
+  gs.approx = list->approx_update != 0;
   if (gs.skip && (reinterpret_cast<uintptr_t>(gs.skip) & 3u)) return PSADAM_ERR_MISALIGNED;
   return PSADAM_OK;
 }

@@ -68,7 +68,7 @@ struct LaunchArgs {
   int static_scales;  // 8-bit: a block's nonzero scale is kept instead of recomputed
   int block_size;     // 8-bit quantization block (the 2048-block kernels assume 2048)
   int tile;           // elements per CTA (a whole number of blocks)
-  int pad_;
+  int approx;         // nonzero: approximate square root and division in the update
   TensorRef t[CAP];
 };
 static_assert(sizeof(LaunchArgs<kCapLarge>) <= 32764, "kernel parameter block too large");

@@ -55,7 +55,7 @@ def _to_dev(arrs, dtype=None):
 
 
 def run_both(psa, mode, sizes, steps, hp, q8=Q8Opts(), grad_dtype="f32", grad_kind="normal", grad_std=1e-2,
-             seed=5, init_state=None):
+             seed=5, init_state=None, approx=False):
     """Run `steps` steps on the GPU and in the oracle from the same inputs; return both."""
     specs = [workloads.TensorSpec(f"t{i}", (n,)) for i, n in enumerate(sizes)]
     p_host = workloads.init_params_np(specs, seed=seed)
@@ -73,7 +73,7 @@ def run_both(psa, mode, sizes, steps, hp, q8=Q8Opts(), grad_dtype="f32", grad_ki
         kw = hp_kwargs(hp)
         if mode in ("q8", "q8v"):
             kw.update(q8_kwargs(q8))
-        psa.adam_step(mode, params, grads, state, t, **kw)
+        psa.adam_step(mode, params, grads, state, t, approx_update=approx, **kw)
         oracle.step_list(mode, p_host, g_host, ostate, t, hp, q8)
     torch.cuda.synchronize()
     got_p = [p.cpu().numpy() for p in params]
@@ -81,23 +81,33 @@ def run_both(psa, mode, sizes, steps, hp, q8=Q8Opts(), grad_dtype="f32", grad_ki
     return got_p, p_host, got_s, ostate
 
 
-def check_all(mode, got_p, want_p, got_s, want_s, what, block_size=oracle.BLOCK):
-    exact = []
+def check_all(mode, got_p, want_p, got_s, want_s, what, block_size=oracle.BLOCK, approx=False):
+    """The contract's tolerances, and beyond them bit for bit: m, v, codes and scales always
+    (they never depend on the update's square root or quotient), the params unless the
+    approximate update ran. That one is checked normwise: its error is a few ulp of the
+    update term, which is not elementwise-relative where a param passes near zero."""
     for i in range(len(got_p)):
-        assert_params(got_p[i], want_p[i], f"{what} tensor {i}")
+        if approx:
+            scale = max(float(np.max(np.abs(want_p[i]), initial=0.0)), 1e-30)
+            err = float(np.max(np.abs(got_p[i].astype(np.float64) - want_p[i]), initial=0.0)) / scale
+            assert err <= 1e-6, f"{what} tensor {i}: params normwise rel err {err:.3g} (approximate update)"
+        else:
+            assert_params(got_p[i], want_p[i], f"{what} tensor {i}")
+            pe = exact_fraction(mode, [got_p[i]], [want_p[i]])
+            assert pe == 1.0, f"{what} tensor {i}: params not bit-identical ({pe})"
         compare_state(mode, got_s[i], want_s[i], f"{what} tensor {i}", block_size)
-        exact.append(exact_fraction(mode, [got_p[i], *got_s[i]], [want_p[i], *want_s[i]]))
-    return min(exact)
+        se = exact_fraction(mode, list(got_s[i]), list(want_s[i]))
+        assert se == 1.0, f"{what} tensor {i}: moments / codes / scales not bit-identical ({se})"
 
 
 # ------------------------------------------------------------------ every mode on ragged lists
+@pytest.mark.parametrize("approx", [False, True])
 @pytest.mark.parametrize("grad_dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("mode", ["fp32", "bf16m"])
-def test_step_ragged_list(psa, mode, grad_dtype):
+def test_step_ragged_list(psa, mode, grad_dtype, approx):
     hp = HParams(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01)
-    got_p, want_p, got_s, want_s = run_both(psa, mode, RAGGED, 5, hp, grad_dtype=grad_dtype)
-    ex = check_all(mode, got_p, want_p, got_s, want_s, f"{mode}/{grad_dtype}")
-    assert ex == 1.0, f"expected bit-identical results, exact fraction {ex}"
+    got_p, want_p, got_s, want_s = run_both(psa, mode, RAGGED, 5, hp, grad_dtype=grad_dtype, approx=approx)
+    check_all(mode, got_p, want_p, got_s, want_s, f"{mode}/{grad_dtype}", approx=approx)
 
 
 Q8_CASES = {
@@ -111,15 +121,15 @@ Q8_CASES = {
 }
 
 
+@pytest.mark.parametrize("approx", [False, True])
 @pytest.mark.parametrize("mode", ["q8", "q8v"])
 @pytest.mark.parametrize("grad_dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("case", sorted(Q8_CASES))
-def test_q8_step_ragged_list(psa, case, grad_dtype, mode):
+def test_q8_step_ragged_list(psa, case, grad_dtype, mode, approx):
     hp = HParams(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.1)
     got_p, want_p, got_s, want_s = run_both(psa, mode, RAGGED, 5, hp, Q8_CASES[case], grad_dtype=grad_dtype,
-                                            grad_kind="student_t_outliers", grad_std=1e-3)
-    ex = check_all(mode, got_p, want_p, got_s, want_s, f"{mode}/{case}/{grad_dtype}")
-    assert ex == 1.0, f"expected bit-identical results, exact fraction {ex}"
+                                            grad_kind="student_t_outliers", grad_std=1e-3, approx=approx)
+    check_all(mode, got_p, want_p, got_s, want_s, f"{mode}/{case}/{grad_dtype}", approx=approx)
 
 
 # ------------------------------------------------------------------ any block size, any percentile
@@ -139,16 +149,16 @@ ANY_CASES = {
 }
 
 
+@pytest.mark.parametrize("approx", [False, True])
 @pytest.mark.parametrize("mode", ["q8", "q8v"])
 @pytest.mark.parametrize("case", sorted(ANY_CASES))
-def test_q8_any_block_size_and_rank(psa, case, mode):
+def test_q8_any_block_size_and_rank(psa, case, mode, approx):
     q8, sizes = ANY_CASES[case]
     hp = HParams(lr=1e-3, weight_decay=0.1)
     gd = "bf16" if case.endswith("sr") else "f32"
     got_p, want_p, got_s, want_s = run_both(psa, mode, sizes, 4, hp, q8, grad_dtype=gd,
-                                            grad_kind="student_t_outliers", grad_std=1e-3)
-    ex = check_all(mode, got_p, want_p, got_s, want_s, f"{mode}/{case}", q8.block_size)
-    assert ex == 1.0, f"expected bit-identical results, exact fraction {ex}"
+                                            grad_kind="student_t_outliers", grad_std=1e-3, approx=approx)
+    check_all(mode, got_p, want_p, got_s, want_s, f"{mode}/{case}", q8.block_size, approx=approx)
 
 
 @pytest.mark.parametrize("case", ["bs1_rne", "bs100_sr_p99", "bs1000_p90", "bs16384_rne", "bs2048_sr_p50"])
@@ -178,6 +188,23 @@ def test_quantize_dequantize_any_block_size(psa, case):
         np.testing.assert_array_equal(back_v[i].cpu().numpy().view(np.uint32), wv.view(np.uint32))
 
 
+@pytest.mark.parametrize("mode", ["fp32", "bf16m", "q8", "q8v"])
+def test_approximate_update_error_is_a_few_ulp(psa, mode):
+    """The opt-in approximate square root and quotient: over 20 steps each param stays
+    within 8 ulp of the update term's size of the IEEE oracle (|p' - p'_oracle| <= 2^-20 *
+    lr/(1-beta1^t) summed over the steps), every moment, code and scale bit-identical."""
+    hp = HParams(lr=1e-3, weight_decay=0.01)
+    steps = 20
+    got_p, want_p, got_s, want_s = run_both(psa, mode, RAGGED, steps, hp, Q8Opts(True, 3, 99.9), grad_std=1e-3,
+                                            approx=True)
+    check_all(mode, got_p, want_p, got_s, want_s, f"{mode} {steps} steps", approx=True)
+    # the update term |lr/bc1 * m/(sqrt(v)/sqrt(bc2) + eps)| is at most about lr/bc1 * 1/sqrt(1-beta2)
+    bound = sum(2.0 ** -20 * hp.lr / (1 - hp.beta1 ** t) / np.sqrt(1 - hp.beta2) for t in range(1, steps + 1))
+    for g, w in zip(got_p, want_p):
+        err = float(np.max(np.abs(g.astype(np.float64) - w), initial=0.0))
+        assert err <= bound, f"{mode}: params max abs err {err:.3g} > {bound:.3g}"
+
+
 def test_zero_grads_are_pure_decay(psa):
     n = 10000
     p0 = workloads.init_params_np([workloads.TensorSpec("w", (n,))], seed=8)[0]
@@ -200,8 +227,7 @@ def test_long_list_spans_several_launches(psa):
     hp = HParams(weight_decay=0.01)
     q8 = Q8Opts(True, 99, 99.9)
     got_p, want_p, got_s, want_s = run_both(psa, "q8", sizes, 2, hp, q8, grad_std=1e-3)
-    ex = check_all("q8", got_p, want_p, got_s, want_s, "q8 long list")
-    assert ex == 1.0
+    check_all("q8", got_p, want_p, got_s, want_s, "q8 long list")
 
 
 # ------------------------------------------------------------------ quantize / dequantize only
