@@ -432,7 +432,8 @@ def main():
         if world == 1 and not args.no_cpu_baseline:
             v, sample = oracle_sample_rate(w, head, args.cpu_seconds)
             cpu = {"value": round(v, 6), "unit": "Gparams/s", "cores": 1, "kind": "oracle", "sample": sample}
-        traffic = ncu_traffic(w.name, head)
+        # the captures are of the plain step; grad zeroing runs another kernel flavour
+        traffic = None if args.zero_grads else ncu_traffic(w.name, head)
         line = {
             "metric": METRIC, "value": round(r["gparams_per_s"], 3), "unit": "Gparams/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(r["ms_per_step"], 5),
