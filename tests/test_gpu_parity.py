@@ -541,3 +541,48 @@ def test_step_plan_matches_direct_calls(psa):
             runs.append([p.cpu().numpy() for p in params])
         for a, b in zip(*runs):
             np.testing.assert_array_equal(a, b)
+
+
+@pytest.mark.parametrize("mode", ["fp32", "bf16m", "q8", "q8v", "q8/bs256"])
+def test_steps_replay_from_a_cuda_graph(psa, mode):
+    """The step calls enqueue kernels only (no host sync, no allocation, no host read of
+    device data), so a stream capture records them: three steps captured into one CUDA graph
+    and replayed equal three direct calls, including the grad check and skip flag."""
+    base, _, bs = mode.partition("/bs")
+    bs = int(bs) if bs else 2048
+    sizes = [3000, 1, 2048 * 2 + 5]
+    specs = [workloads.TensorSpec(f"t{i}", (n,)) for i, n in enumerate(sizes)]
+    p0 = workloads.init_params_np(specs, seed=23)
+    kw = dict(weight_decay=0.01)
+    if base in ("q8", "q8v"):
+        kw.update(stochastic_rounding=True, seed=5, percentile=99.9, block_size=bs)
+    runs = []
+    for use_graph in (False, True):
+        params = _to_dev(p0)
+        state = psa.zeros_state(params, base, bs)
+        gbufs = [_to_dev(workloads.grads_np(sizes, t, 1e-2, seed=23)) for t in (1, 2, 3)]
+        flag = torch.zeros(1, dtype=torch.int32, device=DEV)
+        plans = [psa.StepPlan(base, params, gbufs[t - 1], state, skip_flag=flag, **kw) for t in (1, 2, 3)]
+
+        def three_steps():
+            for t in (1, 2, 3):
+                psa.check_grads(gbufs[t - 1], flag)
+                plans[t - 1].step(t)
+
+        if use_graph:
+            side = torch.cuda.Stream()
+            side.wait_stream(torch.cuda.current_stream())
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(side):
+                with torch.cuda.graph(g, stream=side):
+                    three_steps()
+            torch.cuda.current_stream().wait_stream(side)
+            g.replay()
+        else:
+            three_steps()
+        torch.cuda.synchronize()
+        runs.append([p.cpu().numpy() for p in params] + [s.cpu().numpy() if s.dtype != torch.bfloat16 else
+                                                          s.view(torch.int16).cpu().numpy()
+                                                          for part in state for s in part])
+    for a, b in zip(*runs):
+        np.testing.assert_array_equal(a, b)
