@@ -269,22 +269,30 @@ def run_ours(args, rank: int, world: int, dist):
 
 
 def run_e2e(args, psa, torch, dev, stream, w, params, state, kw, t, flush, dist, world):
+    """The step through the public API with host buffers: every step copies its grads from
+    pinned host memory and the updated params back, inside the timed span. One call per step,
+    StepPlan.step_from_host: the library cuts the list into block-aligned chunks whose
+    uploads, steps and downloads overlap on three streams (bit for bit the one-call step)."""
     sizes = w.sizes
+    mode, over = parse_mode(args.modes[0])
     gdt = torch.float32 if w.grad_dtype == "f32" else torch.bfloat16
     host_g = [workloads.grads_torch(sizes, s + 1, w.grad_std, dev, dtype=w.grad_dtype) for s in range(2)]
     host_g = [[g.cpu().pin_memory() for g in gs] for gs in host_g]
     host_p = [torch.empty(p.numel(), dtype=torch.float32, pin_memory=True) for p in params]
     dev_g = [torch.empty(n, dtype=gdt, device=dev) for n in sizes]
-    plan = psa.StepPlan(parse_mode(args.modes[0])[0], params, dev_g, state, **kw)
     h2d = sum(g.numel() * g.element_size() for g in host_g[0])
     d2h = sum(p.numel() * 4 for p in params)
+    plan = psa.StepPlan(mode, params, dev_g, state, **kw)
+    piped = args.e2e_chunks > 1
+    s_in, s_out = (torch.cuda.Stream(dev), torch.cuda.Stream(dev)) if piped else (None, None)
+
+    def one_step(k, tt):
+        plan.step_from_host(tt, host_g[k], host_p, n_chunks=args.e2e_chunks, stream=stream, stream_in=s_in,
+                            stream_out=s_out)
+
     for i in range(3):  # warm the copy engines
         t += 1
-        for d, h in zip(dev_g, host_g[i % 2]):
-            d.copy_(h, non_blocking=True)
-        plan.step(t)
-        for h, p in zip(host_p, params):
-            h.copy_(p, non_blocking=True)
+        one_step(i % 2, t)
     torch.cuda.synchronize(dev)
     if dist is not None:
         dist.barrier()
@@ -295,17 +303,15 @@ def run_e2e(args, psa, torch, dev, stream, w, params, state, kw, t, flush, dist,
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        for d, h in zip(dev_g, host_g[i % 2]):
-            d.copy_(h, non_blocking=True)
-        plan.step(t)
-        for h, p in zip(host_p, params):
-            h.copy_(p, non_blocking=True)
+        one_step(i % 2, t)
         e1.record(stream)
         e1.synchronize()
         ms.append(e0.elapsed_time(e1))
     total_s = max_over_ranks(sum(ms) / 1e3, dist, dev)
     return {"value": round(job_gparams_per_s(sum(sizes), args.steps, total_s, world), 3), "unit": "Gparams/s",
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "pipeline": f"psadam_step_from_host, {args.e2e_chunks} chunks on 3 streams" if piped else
+                        "psadam_step_from_host, one stream"}
 
 
 # ------------------------------------------------------------------ the CPU oracle as a baseline
@@ -386,6 +392,8 @@ def main():
     ap.add_argument("--zero-grads", action="store_true",
                     help="zero the grads inside the step (adds a grad write per param)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-chunks", type=int, default=8,
+                    help="end-to-end leg: chunks whose copies overlap the step (1 = one stream, in series)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-step-seconds", type=float, default=3.0)
     args = ap.parse_args()

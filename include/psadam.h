@@ -158,6 +158,24 @@ int adam_step_q8(const psadam_list* list, int8_t* const* m_code, uint8_t* const*
 int adam_step_q8v(const psadam_list* list, float* const* m, uint8_t* const* v_code, float* const* v_scale,
                   int64_t step, const psadam_hparams* hp, const psadam_q8_opts* q8, void* stream);
 
+/* One step with host-resident grads and params (the end-to-end form of a step): copies each
+ * grad from host_grad[i] (host memory, page-locked for asynchronous copies; fp32 or bf16 per
+ * list->grad_dtype) into list->grad[i], steps, and copies the updated list->param[i] back to
+ * host_param[i] (host fp32). mode: 0 fp32, 1 bf16m, 2 8-bit, 3 fp32 m + 8-bit v, with m, v,
+ * m_scale, v_scale the arrays the matching adam_step_* call takes (NULL where that call has
+ * none; q8 options only for modes 2 and 3). With stream_in and stream_out (two streams other
+ * than `stream`) the list is cut into about n_chunks chunks (whole tensors; a larger tensor
+ * at multiples of 4 quantization blocks and 16 elements) whose uploads (stream_in), steps
+ * (stream) and downloads (stream_out) overlap; NULL streams run it all on `stream`. Either
+ * way the results are bit for bit those of one adam_step_* call over the whole list (a
+ * slice keeps its tensor's element offsets and list position for stochastic rounding), and
+ * `stream` is ordered after every copy when the call returns. */
+int psadam_step_from_host(int32_t mode, const psadam_list* list, const void* const* host_grad,
+                          float* const* host_param, void* const* m, void* const* v,
+                          float* const* m_scale, float* const* v_scale, int64_t step,
+                          const psadam_hparams* hp, const psadam_q8_opts* q8, int32_t n_chunks,
+                          void* stream, void* stream_in, void* stream_out);
+
 /* Quantize-only (PR #814's Quantize(m), Quantize(v)): encodes fp32 m, v into codes and
  * scales exactly as adam_step_q8 encodes m', v' (same rounding, percentile and, for
  * stochastic rounding, the same Philox stream for `step`). For state initialisation

@@ -70,6 +70,8 @@ _SIGS = {
                            ctypes.c_int64, _vp],
     "psadam_q8_dequantize": [ctypes.c_int32, _I64P, _PP, _PP, _PP, _PP, _PP, _PP, ctypes.c_int32, _vp],
     "psadam_check_grads": [ctypes.POINTER(_List), _vp, _vp],
+    "psadam_step_from_host": [ctypes.c_int32, ctypes.POINTER(_List), _PP, _PP, _PP, _PP, _PP, _PP, ctypes.c_int64,
+                              ctypes.POINTER(_HParams), ctypes.POINTER(_Q8Opts), ctypes.c_int32, _vp, _vp, _vp],
 }
 for _name, _args in _SIGS.items():
     getattr(_lib, _name).argtypes = _args
@@ -397,6 +399,40 @@ class StepPlan:
             st = _lib.adam_step_q8v(ctypes.byref(self._lst), *self._state_pp, step, ctypes.byref(self._hp),
                                     ctypes.byref(self._q8), h)
         _raise(st, f"StepPlan.step ({self.mode})")
+
+    def step_from_host(self, step: int, host_grads, host_params, n_chunks: int = 4, stream=None, stream_in=None,
+                       stream_out=None) -> None:
+        """The step with host-resident grads and params: ``host_grads`` (CPU tensors like the
+        plan's grads, pinned for asynchronous copies) are copied into the plan's device grads,
+        the step runs, and the updated params are copied into ``host_params`` (CPU float32).
+        With ``stream_in`` and ``stream_out`` the list is cut into about ``n_chunks`` chunks whose
+        copies overlap the step; results equal :meth:`step` bit for bit."""
+        if len(host_grads) != len(self._params) or len(host_params) != len(self._params):
+            raise ValueError("host grads / params differ in length from params")
+        for i, (hg, hp, p) in enumerate(zip(host_grads, host_params, self._params)):
+            if hg.is_cuda or hp.is_cuda:
+                raise TypeError(f"host tensor {i} is on a CUDA device")
+            if hg.dtype != self._grad_dtype or hp.dtype != torch.float32:
+                raise TypeError(f"host tensor {i}: expected grads {self._grad_dtype} and params float32")
+            if hg.numel() != p.numel() or hp.numel() != p.numel() or not hg.is_contiguous() or not hp.is_contiguous():
+                raise ValueError(f"host tensor {i}: expected {p.numel()} contiguous elements")
+        key = (tuple(t.data_ptr() for t in host_grads), tuple(t.data_ptr() for t in host_params))
+        if getattr(self, "_host_key", None) != key:
+            self._host_key = key
+            self._host_tables = (_ptrs(host_grads), _ptrs(host_params))
+        hg, hp = self._host_tables
+        n_state = len(self._state_pp)
+        pp = list(self._state_pp) + [None] * (4 - n_state)
+        if self.mode == "q8v":  # (m, v codes, v scale) -> m, v, no m scale, v scale
+            pp = [self._state_pp[0], self._state_pp[1], None, self._state_pp[2]]
+        h = _stream_handle(stream, self._params)
+        sin = _stream_handle(stream_in, self._params) if stream_in is not None else None
+        sout = _stream_handle(stream_out, self._params) if stream_out is not None else None
+        q8 = ctypes.byref(self._q8) if self.mode in ("q8", "q8v") else None
+        st = _lib.psadam_step_from_host(MODES[self.mode], ctypes.byref(self._lst), ctypes.cast(hg, _PP),
+                                        ctypes.cast(hp, _PP), *pp, step, ctypes.byref(self._hp), q8, n_chunks, h,
+                                        sin, sout)
+        _raise(st, f"StepPlan.step_from_host ({self.mode})")
 
 
 def cdll() -> ctypes.CDLL:

@@ -31,6 +31,7 @@ struct Entry {
   float* vs;
   long long numel;
   int list_idx;
+  long long elem_off = 0;  // a slice's first element within its whole tensor (a multiple of 4)
 };
 
 int check_hparams(const psadam_hparams* hp, int64_t step) {
@@ -170,6 +171,7 @@ int run_launches(const std::vector<Entry>& es, const StepConsts& c, uint64_t see
       t.block_begin = (int)blocks;
       t.k_last = percentile_rank(pct, last_block_len(es[i].numel, bs));
       t.list_idx = es[i].list_idx;
+      t.grp_off = (int)(es[i].elem_off / 4);
       blocks += nb;
       ++i;
     }
@@ -269,41 +271,200 @@ int collect_list(const psadam_list* list, const void* const* m, const void* cons
   return PSADAM_OK;
 }
 
+// A validated step: everything the launches need.
+struct StepCall {
+  int mode = 0;
+  bool q8mode = false, sr = false, gb = false;
+  float pct = 100.f;
+  uint64_t seed = 0;
+  int bs = kBlock;
+  GradSide gs;
+  StepConsts c{};
+  int64_t step = 1;
+};
+
+int prepare_step(int mode, const psadam_list* list, const void* const* m, const void* const* v, const float* const* ms,
+                 const float* const* vs, int64_t step, const psadam_hparams* hp, const psadam_q8_opts* q8,
+                 std::vector<Entry>& es, StepCall& call) {
+  int st = check_hparams(hp, step);
+  if (st != PSADAM_OK) return st;
+  call.mode = mode;
+  call.q8mode = mode == kModeQ8 || mode == kModeQ8V;
+  if (call.q8mode && (st = check_q8(q8)) != PSADAM_OK) return st;
+  if ((st = collect_list(list, m, v, ms, vs, mode == kModeQ8, call.q8mode, es)) != PSADAM_OK) return st;
+  call.pct = call.q8mode ? q8->percentile : 100.f;
+  call.sr = call.q8mode && q8->stochastic_rounding;
+  call.seed = call.q8mode ? q8->seed : 0;
+  call.bs = call.q8mode ? q8->block_size : kBlock;
+  if ((st = check_block_counts(es, call.bs)) != PSADAM_OK) return st;
+  if ((st = grad_side(list, call.gs)) != PSADAM_OK) return st;
+  call.gs.static_scales = call.q8mode && q8->static_scales != 0;
+  call.gb = list->grad_dtype == PSADAM_GRAD_BF16;
+  call.c = make_consts(*hp, step);
+  call.step = step;
+  return PSADAM_OK;
+}
+
+// Launch the step over es (the whole list, or slices of it: every per-block decision below
+// depends only on each block's own elements, its tensor's last-block length and rank).
+int launch_prepared(const std::vector<Entry>& es, const StepCall& call, cudaStream_t s) {
+  const int kmax = max_rank(es, call.pct, call.bs);
+  // 2048-element blocks with rank <= kMaxRank: the specialised kernels; otherwise the general one
+  if (call.q8mode && (call.bs != kBlock || kmax > kMaxRank))
+    return dispatch(es, call.c, call.seed, call.step, call.pct, pick_step_any<kCapSmall>(call.mode, call.gb, call.sr),
+                    pick_step_any<kCapLarge>(call.mode, call.gb, call.sr), s, call.gs, call.bs, any_tile(call.bs));
+  const int K = rank_template(kmax);
+  return dispatch(es, call.c, call.seed, call.step, call.pct, pick_step<kCapSmall>(call.mode, call.gb, call.sr, K),
+                  pick_step<kCapLarge>(call.mode, call.gb, call.sr, K), s, call.gs);
+}
+
 int step_common(int mode, const psadam_list* list, const void* const* m, const void* const* v,
                 const float* const* ms, const float* const* vs, int64_t step, const psadam_hparams* hp,
                 const psadam_q8_opts* q8, void* stream) {
   if (!list || list->n_tensors < 0) return PSADAM_ERR_INVALID_ARG;
   if (list->n_tensors == 0) return PSADAM_OK;
-  int st = check_hparams(hp, step);
-  if (st != PSADAM_OK) return st;
-  const bool q8mode = mode == kModeQ8 || mode == kModeQ8V;
-  if (q8mode && (st = check_q8(q8)) != PSADAM_OK) return st;
   std::vector<Entry> es;
-  if ((st = collect_list(list, m, v, ms, vs, mode == kModeQ8, q8mode, es)) != PSADAM_OK) return st;
-  const float pct = q8mode ? q8->percentile : 100.f;
-  const bool sr = q8mode && q8->stochastic_rounding;
-  const uint64_t seed = q8mode ? q8->seed : 0;
-  const int bs = q8mode ? q8->block_size : kBlock;
-  if ((st = check_block_counts(es, bs)) != PSADAM_OK) return st;
-  const int kmax = max_rank(es, pct, bs);
-  GradSide gs;
-  if ((st = grad_side(list, gs)) != PSADAM_OK) return st;
-  gs.static_scales = q8mode && q8->static_scales != 0;
-  const bool gb = list->grad_dtype == PSADAM_GRAD_BF16;
-  const StepConsts c = make_consts(*hp, step);
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // 2048-element blocks with rank <= 16: the specialised kernels; otherwise one CTA per block
-  if (q8mode && (bs != kBlock || kmax > kMaxRank))
-    return dispatch(es, c, seed, step, pct, pick_step_any<kCapSmall>(mode, gb, sr), pick_step_any<kCapLarge>(mode, gb, sr),
-                    s, gs, bs, any_tile(bs));
-  const int K = rank_template(kmax);
-  return dispatch(es, c, seed, step, pct, pick_step<kCapSmall>(mode, gb, sr, K), pick_step<kCapLarge>(mode, gb, sr, K),
-                  s, gs);
+  StepCall call;
+  const int st = prepare_step(mode, list, m, v, ms, vs, step, hp, q8, es, call);
+  if (st != PSADAM_OK) return st;
+  return launch_prepared(es, call, static_cast<cudaStream_t>(stream));
+}
+
+// Events for the host pipeline, created once per thread and reused.
+struct EventPool {
+  std::vector<cudaEvent_t> ev;
+  ~EventPool() {
+    for (cudaEvent_t e : ev) cudaEventDestroy(e);
+  }
+  cudaError_t get(size_t n, cudaEvent_t** out) {
+    while (ev.size() < n) {
+      cudaEvent_t e;
+      const cudaError_t err = cudaEventCreateWithFlags(&e, cudaEventDisableTiming);
+      if (err != cudaSuccess) return err;
+      ev.push_back(e);
+    }
+    *out = ev.data();
+    return cudaSuccess;
+  }
+};
+
+int cuda_fail(cudaError_t e) {
+  g_last_cuda_error = (int32_t)e;
+  return PSADAM_ERR_CUDA;
+}
+
+// The list cut into chunks of about total/n_chunks elements: whole tensors in order, a tensor
+// that does not fit the current chunk cut at a multiple of `unit` elements from its start.
+std::vector<std::vector<Entry>> make_chunks(const std::vector<Entry>& es, int n_chunks, long long unit, int mode,
+                                            int bs, size_t grad_bytes) {
+  long long total = 0;
+  for (const Entry& e : es) total += e.numel;
+  long long target = (total / n_chunks + unit - 1) / unit * unit;
+  if (target < unit) target = unit;
+  const int mb = mode == kModeF32 || mode == kModeQ8V ? 4 : (mode == kModeBF16 ? 2 : 1);  // m bytes / element
+  const int vb = mode == kModeF32 ? 4 : (mode == kModeBF16 ? 2 : 1);
+  std::vector<std::vector<Entry>> chunks(1);
+  long long size = 0;
+  for (const Entry& e : es) {
+    long long lo = 0;
+    while (lo < e.numel) {
+      long long hi = e.numel - lo <= target - size ? e.numel : lo + (target - size) / unit * unit;
+      if (hi <= lo) {  // not even one unit fits: close the chunk first
+        chunks.emplace_back();
+        size = 0;
+        continue;
+      }
+      Entry piece = e;
+      piece.p = e.p + lo;
+      piece.g = static_cast<const char*>(e.g) + lo * (long long)grad_bytes;
+      piece.m = static_cast<char*>(e.m) + lo * mb;
+      piece.v = static_cast<char*>(e.v) + lo * vb;
+      piece.ms = e.ms ? e.ms + lo / bs : nullptr;
+      piece.vs = e.vs ? e.vs + lo / bs : nullptr;
+      piece.numel = hi - lo;
+      piece.elem_off = e.elem_off + lo;
+      chunks.back().push_back(piece);
+      size += hi - lo;
+      lo = hi;
+      if (size >= target || lo < e.numel) {
+        chunks.emplace_back();
+        size = 0;
+      }
+    }
+  }
+  if (chunks.back().empty()) chunks.pop_back();
+  return chunks;
 }
 
 }  // namespace
 
 extern "C" {
+
+int psadam_step_from_host(int32_t mode, const psadam_list* list, const void* const* host_grad, float* const* host_param,
+                          void* const* m, void* const* v, float* const* m_scale, float* const* v_scale, int64_t step,
+                          const psadam_hparams* hp, const psadam_q8_opts* q8, int32_t n_chunks, void* stream,
+                          void* stream_in, void* stream_out) {
+  if (mode < kModeF32 || mode > kModeQ8V || !list || list->n_tensors < 0 || n_chunks < 1)
+    return PSADAM_ERR_INVALID_ARG;
+  if (list->n_tensors == 0) return PSADAM_OK;
+  if (!host_grad || !host_param) return PSADAM_ERR_INVALID_ARG;
+  for (int i = 0; i < list->n_tensors; ++i)
+    if (list->numel && list->numel[i] > 0 && (!host_grad[i] || !host_param[i])) return PSADAM_ERR_INVALID_ARG;
+  std::vector<Entry> es;
+  StepCall call;
+  int st = prepare_step(mode, list, reinterpret_cast<const void* const*>(m), reinterpret_cast<const void* const*>(v),
+                        m_scale, v_scale, step, hp, q8, es, call);
+  if (st != PSADAM_OK) return st;
+  if (es.empty()) return PSADAM_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const bool piped = stream_in != nullptr && stream_out != nullptr;
+  cudaStream_t sin = piped ? static_cast<cudaStream_t>(stream_in) : s;
+  cudaStream_t sout = piped ? static_cast<cudaStream_t>(stream_out) : s;
+  const size_t gsz = call.gb ? 2 : 4;
+  // cut points keep every slice 16-byte aligned: a multiple of 4 blocks (scales) and of 16
+  // elements (8-bit codes)
+  long long unit = 4LL * call.bs;
+  while (unit % 16 != 0) unit *= 2;
+  const std::vector<std::vector<Entry>> chunks = make_chunks(es, piped ? n_chunks : 1, unit, mode, call.bs, gsz);
+  static thread_local EventPool pool;
+  cudaEvent_t* ev = nullptr;
+  cudaError_t e = pool.get(2 * chunks.size() + 2, &ev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  // the uploads overwrite the device grads: they wait for the caller's earlier work
+  if (piped) {
+    if ((e = cudaEventRecord(ev[0], s)) != cudaSuccess || (e = cudaStreamWaitEvent(sin, ev[0], 0)) != cudaSuccess)
+      return cuda_fail(e);
+  }
+  for (size_t c = 0; c < chunks.size(); ++c) {
+    for (const Entry& pc : chunks[c]) {
+      const char* src = static_cast<const char*>(host_grad[pc.list_idx]) + pc.elem_off * (long long)gsz;
+      if ((e = cudaMemcpyAsync(const_cast<void*>(pc.g), src, pc.numel * gsz, cudaMemcpyHostToDevice, sin)) != cudaSuccess)
+        return cuda_fail(e);
+    }
+    if (piped) {
+      if ((e = cudaEventRecord(ev[2 + 2 * c], sin)) != cudaSuccess || (e = cudaStreamWaitEvent(s, ev[2 + 2 * c], 0)) != cudaSuccess)
+        return cuda_fail(e);
+    }
+    if ((st = launch_prepared(chunks[c], call, s)) != PSADAM_OK) return st;
+    if (piped) {
+      if ((e = cudaEventRecord(ev[3 + 2 * c], s)) != cudaSuccess ||
+          (e = cudaStreamWaitEvent(sout, ev[3 + 2 * c], 0)) != cudaSuccess)
+        return cuda_fail(e);
+    }
+    for (const Entry& pc : chunks[c]) {
+      float* dst = host_param[pc.list_idx] + pc.elem_off;
+      if ((e = cudaMemcpyAsync(dst, pc.p, pc.numel * sizeof(float), cudaMemcpyDeviceToHost, sout)) != cudaSuccess)
+        return cuda_fail(e);
+    }
+  }
+  // the caller's stream sees the whole step, downloads included
+  if (piped) {
+    if ((e = cudaEventRecord(ev[1], sout)) != cudaSuccess || (e = cudaStreamWaitEvent(s, ev[1], 0)) != cudaSuccess)
+      return cuda_fail(e);
+  }
+  return PSADAM_OK;
+}
+
 
 int adam_step_fp32(const psadam_list* list, float* const* m, float* const* v, int64_t step,
                    const psadam_hparams* hp, void* stream) {

@@ -52,7 +52,8 @@ struct TensorRef {
   int block_begin;  // index of this tensor's first CTA within the launch
   int k_last;       // percentile rank of the tensor's last block (may be partial)
   int list_idx;     // position in the caller's list (stochastic-rounding stream)
-  int pad_;
+  int grp_off;      // first element / 4 within the caller's whole tensor (nonzero for a slice
+                    // of one): added to the stochastic-rounding counter
 };
 
 template <int CAP>

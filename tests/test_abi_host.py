@@ -30,7 +30,8 @@ def declared_functions():
 def test_header_declares_the_step_entry_points():
     names = declared_functions()
     for want in ("adam_step_fp32", "adam_step_bf16m", "adam_step_q8", "adam_step_q8v", "psadam_q8_quantize",
-                 "psadam_q8_dequantize", "psadam_state_bytes", "psadam_status_string"):
+                 "psadam_q8_dequantize", "psadam_state_bytes", "psadam_status_string", "psadam_check_grads",
+                 "psadam_step_from_host"):
         assert want in names
 
 
@@ -141,3 +142,25 @@ def test_dequantize_block_size_validation(psa):
     assert lib.psadam_q8_dequantize(1, nums, P, P, P, P, P, P, 0, None) == psa.ERR_INVALID_ARG
     assert lib.psadam_q8_dequantize(1, nums, P, P, P, P, P, P, 16385, None) == psa.ERR_UNSUPPORTED
     assert lib.psadam_q8_dequantize(0, nums, P, P, P, P, P, P, 0, None) == psa.OK  # empty list: no-op
+
+
+def test_step_from_host_validation(psa):
+    """Every argument error is reported before a copy or a launch is enqueued."""
+    C = ctypes
+    nums = _arr(C.c_int64, [4096])
+    P = C.cast(_arr(C.c_void_p, [FAKE]), psa._PP)
+    lst = psa._List(1, 0, nums, P, P, 1.0, 0, None, 0)
+    hp = psa._HParams(1e-3, 0.9, 0.999, 1e-8, 0.0)
+    q = psa._Q8Opts(2048, 0, 42, 100.0)
+    lib = psa.cdll()
+    f = lib.psadam_step_from_host
+    B = C.byref
+    assert f(7, B(lst), P, P, P, P, P, P, 1, B(hp), B(q), 4, None, None, None) == psa.ERR_INVALID_ARG      # mode
+    assert f(2, B(lst), P, P, P, P, P, P, 1, B(hp), B(q), 0, None, None, None) == psa.ERR_INVALID_ARG      # chunks
+    assert f(2, B(lst), None, P, P, P, P, P, 1, B(hp), B(q), 4, None, None, None) == psa.ERR_INVALID_ARG   # host grads
+    assert f(2, B(lst), P, P, P, P, P, P, 0, B(hp), B(q), 4, None, None, None) == psa.ERR_INVALID_ARG      # step
+    assert f(2, B(lst), P, P, P, P, P, P, 1, B(hp), None, 4, None, None, None) == psa.ERR_INVALID_ARG      # q8 opts
+    bad = C.cast(_arr(C.c_void_p, [FAKE + 8]), psa._PP)
+    assert f(2, B(lst), P, P, bad, P, P, P, 1, B(hp), B(q), 4, None, None, None) == psa.ERR_MISALIGNED
+    empty = psa._List(0, 0, nums, P, P, 1.0, 0, None, 0)
+    assert f(2, B(empty), None, None, None, None, None, None, 1, B(hp), B(q), 4, None, None, None) == psa.OK

@@ -586,3 +586,53 @@ def test_steps_replay_from_a_cuda_graph(psa, mode):
                                                           for part in state for s in part])
     for a, b in zip(*runs):
         np.testing.assert_array_equal(a, b)
+
+
+@pytest.mark.parametrize("piped", [False, True])
+@pytest.mark.parametrize("mode", ["fp32", "bf16m", "q8", "q8v", "q8/bs256", "q8/p99"])
+def test_step_from_host_equals_device_step(psa, mode, piped):
+    """psadam_step_from_host (grads uploaded from pinned host buffers, params downloaded), in
+    chunks pipelined over three streams or in one piece: the same bits as device-resident steps,
+    with stochastic rounding (slices keep their tensors' element offsets and list positions)."""
+    base, _, rest = mode.partition("/")
+    kw = dict(weight_decay=0.01)
+    if base in ("q8", "q8v"):
+        kw.update(stochastic_rounding=True, seed=9, percentile=99.9)
+        if rest.startswith("bs"):
+            kw["block_size"] = int(rest[2:])
+        elif rest.startswith("p"):
+            kw["percentile"] = float(rest[1:])
+    bs = kw.get("block_size", 2048)
+    sizes = [3000, 1, 2048 * 40 + 7, 70001, 0]
+    specs = [workloads.TensorSpec(f"t{i}", (n,)) for i, n in enumerate(sizes)]
+    p0 = workloads.init_params_np(specs, seed=29)
+    gdt = torch.bfloat16 if base == "bf16m" else torch.float32
+    host_grads = []
+    for t in (1, 2, 3):
+        g = [torch.from_numpy(x) for x in workloads.grads_np(sizes, t, 1e-2, seed=29)]
+        host_grads.append([x.to(gdt).pin_memory() for x in g])
+    runs = []
+    for from_host in (False, True):
+        params = _to_dev(p0)
+        state = psa.zeros_state(params, base, bs)
+        dev_g = [torch.empty(n, dtype=gdt, device=DEV) for n in sizes]
+        plan = psa.StepPlan(base, params, dev_g, state, **kw)
+        out = [torch.empty(n, dtype=torch.float32).pin_memory() for n in sizes]
+        s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+        for t in (1, 2, 3):
+            if from_host:
+                plan.step_from_host(t, host_grads[t - 1], out, n_chunks=5,
+                                    stream_in=s_in if piped else None, stream_out=s_out if piped else None)
+            else:
+                for d, h in zip(dev_g, host_grads[t - 1]):
+                    d.copy_(h)
+                plan.step(t)
+        torch.cuda.synchronize()
+        got = [p.cpu().numpy() for p in params]
+        if from_host:
+            for a, b in zip(got, out):
+                np.testing.assert_array_equal(a, b.numpy())
+        runs.append(got + [(s.view(torch.int16) if s.dtype == torch.bfloat16 else s).cpu().numpy()
+                           for part in state for s in part])
+    for a, b in zip(*runs):
+        np.testing.assert_array_equal(a, b)
