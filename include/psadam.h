@@ -60,6 +60,7 @@
  *     returns the cudaError_t value.
  *   - The library allocates no device memory: tensor metadata travels as kernel
  *     parameters; lists longer than one launch can carry are split into several launches.
+ *     (psadam_step_from_host keeps a per-thread pool of CUDA events, created on first use.)
  */
 #ifndef PSADAM_H
 #define PSADAM_H
