@@ -26,7 +26,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libpsadam.so")
 BLOCK = 2048             # the 8-bit format's default block (the specialised kernels' size)
 MAX_BLOCK = 16384        # largest block size the library accepts
-MAX_PERCENTILE_RANK = 16 # above this rank (or at another block size) the general kernel runs
+MAX_PERCENTILE_RANK = 4  # above this rank (or at another block size) the general kernel runs
 
 OK, ERR_INVALID_ARG, ERR_MISALIGNED, ERR_UNSUPPORTED, ERR_CUDA = range(5)
 GRAD_F32, GRAD_BF16 = 0, 1
