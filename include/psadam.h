@@ -206,6 +206,11 @@ int psadam_check_grads(const psadam_list* list, int32_t* found_nonfinite, void* 
  * Returns 0 for an unknown mode, numel < 0, or B < 1 in modes 2 and 3. */
 size_t psadam_state_bytes(int32_t mode, int64_t numel, int32_t block_size);
 
+/* 1 if a kernel of the library gave up a bounded wait on its own asynchronous copies since
+ * the last call (its results are then not to be trusted), 0 if not, -1 if the device could
+ * not be queried; reading clears it. Synchronises with the device. */
+int32_t psadam_device_fault(void);
+
 /* Static, human-readable name of a psadam_status value. */
 const char* psadam_status_string(int32_t status);
 

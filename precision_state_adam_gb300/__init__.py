@@ -80,6 +80,8 @@ _lib.psadam_state_bytes.argtypes = [ctypes.c_int32, ctypes.c_int64, ctypes.c_int
 _lib.psadam_state_bytes.restype = ctypes.c_size_t
 _lib.psadam_status_string.argtypes = [ctypes.c_int32]
 _lib.psadam_status_string.restype = ctypes.c_char_p
+_lib.psadam_device_fault.argtypes = []
+_lib.psadam_device_fault.restype = ctypes.c_int32
 _lib.psadam_last_cuda_error.argtypes = []
 _lib.psadam_last_cuda_error.restype = ctypes.c_int32
 
@@ -433,6 +435,11 @@ class StepPlan:
                                         ctypes.cast(hp, _PP), *pp, step, ctypes.byref(self._hp), q8, n_chunks, h,
                                         sin, sout)
         _raise(st, f"StepPlan.step_from_host ({self.mode})")
+
+
+def device_fault() -> int:
+    """1 if a library kernel gave up a bounded wait since the last call (then read as 0), else 0."""
+    return int(_lib.psadam_device_fault())
 
 
 def cdll() -> ctypes.CDLL:

@@ -1,6 +1,7 @@
 // psadam_api.cu — the C ABI declared in include/psadam.h: argument validation, the
 // per-step constants, tensor-list packing into launch-parameter blocks, and dispatch to
 // the kernel instantiations. No device memory is allocated here.
+#include <atomic>
 #include <climits>
 #include <cmath>
 #include <cstdint>
@@ -12,9 +13,29 @@
 
 using namespace psadam;
 
+// Set to 1 by a kernel whose bounded wait gave up (read and cleared by psadam_device_fault).
+// A module variable: the library still allocates no device memory.
+__device__ int g_psadam_fault = 0;
+
 namespace {
 
 thread_local int32_t g_last_cuda_error = 0;
+
+// Device address of g_psadam_fault on the current device (looked up once per device).
+int* fault_word() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+  constexpr int kMaxDev = 64;
+  static std::atomic<int*> cache[kMaxDev];
+  if (dev < kMaxDev) {
+    int* p = cache[dev].load(std::memory_order_relaxed);
+    if (p) return p;
+  }
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_psadam_fault) != cudaSuccess) return nullptr;
+  if (dev < kMaxDev) cache[dev].store(static_cast<int*>(p), std::memory_order_relaxed);
+  return static_cast<int*>(p);
+}
 
 // Largest tensor whose block count fits a grid dimension.
 constexpr long long kMaxNumel = (long long)INT_MAX * kBlock;
@@ -147,6 +168,7 @@ int run_launches(const std::vector<Entry>& es, const StepConsts& c, uint64_t see
   a.skip = gs.skip;
   a.static_scales = gs.static_scales;
   a.approx = gs.approx;
+  a.fault = fault_word();
   a.seed_lo = (uint32_t)(seed & 0xFFFFFFFFu);
   a.seed_hi = (uint32_t)(seed >> 32);
   a.step_lo = (uint32_t)step;
@@ -591,6 +613,16 @@ size_t psadam_state_bytes(int32_t mode, int64_t numel, int32_t block_size) {
     case 3: return 5 * n + 4 * (size_t)n_blocks(numel, block_size);
     default: return 0;
   }
+}
+
+int32_t psadam_device_fault(void) {
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_psadam_fault, sizeof v) != cudaSuccess) return -1;
+  if (v != 0) {
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_psadam_fault, &zero, sizeof zero) != cudaSuccess) return -1;
+  }
+  return v;
 }
 
 const char* psadam_status_string(int32_t status) {

@@ -66,6 +66,7 @@ struct LaunchArgs {
   float g_unscale;  // grads are multiplied by this before use (1: unchanged)
   int zero_grads;   // nonzero: overwrite each grad with zero after reading it
   const int* skip;  // device flag or null: a nonzero value makes the launch a no-op
+  int* fault;       // device word set to 1 when a bounded wait gives up (see psadam_device_fault)
   int static_scales;  // 8-bit: a block's nonzero scale is kept instead of recomputed
   int block_size;     // 8-bit quantization block (the 2048-block kernels assume 2048)
   int tile;           // elements per CTA (a whole number of blocks)
