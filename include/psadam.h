@@ -211,6 +211,11 @@ size_t psadam_state_bytes(int32_t mode, int64_t numel, int32_t block_size);
  * not be queried; reading clears it. Synchronises with the device. */
 int32_t psadam_device_fault(void);
 
+/* Self-test of the failure path above: one thread waits on a barrier that nothing completes,
+ * gives up after `cycles` SM cycles and sets the fault word (so the next
+ * psadam_device_fault() returns 1). It never faults or hangs the device. */
+int psadam_selftest_bounded_wait(int64_t cycles, void* stream);
+
 /* Static, human-readable name of a psadam_status value. */
 const char* psadam_status_string(int32_t status);
 

@@ -80,6 +80,8 @@ _lib.psadam_state_bytes.argtypes = [ctypes.c_int32, ctypes.c_int64, ctypes.c_int
 _lib.psadam_state_bytes.restype = ctypes.c_size_t
 _lib.psadam_status_string.argtypes = [ctypes.c_int32]
 _lib.psadam_status_string.restype = ctypes.c_char_p
+_lib.psadam_selftest_bounded_wait.argtypes = [ctypes.c_int64, ctypes.c_void_p]
+_lib.psadam_selftest_bounded_wait.restype = ctypes.c_int
 _lib.psadam_device_fault.argtypes = []
 _lib.psadam_device_fault.restype = ctypes.c_int32
 _lib.psadam_last_cuda_error.argtypes = []

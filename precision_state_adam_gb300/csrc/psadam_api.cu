@@ -615,6 +615,14 @@ size_t psadam_state_bytes(int32_t mode, int64_t numel, int32_t block_size) {
   }
 }
 
+int psadam_selftest_bounded_wait(int64_t cycles, void* stream) {
+  if (cycles < 0) return PSADAM_ERR_INVALID_ARG;
+  int* fault = fault_word();
+  if (fault == nullptr) return PSADAM_ERR_CUDA;
+  const cudaError_t e = launch_wait_selftest(fault, cycles, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PSADAM_OK : cuda_fail(e);
+}
+
 int32_t psadam_device_fault(void) {
   int v = 0;
   if (cudaMemcpyFromSymbol(&v, g_psadam_fault, sizeof v) != cudaSuccess) return -1;

@@ -98,6 +98,9 @@ cudaError_t launch_quantize_any(const LaunchArgs<CAP>& a, cudaStream_t s);
 template <int CAP>
 cudaError_t launch_dequantize_any(const LaunchArgs<CAP>& a, cudaStream_t s);
 
+// Bounded-wait self-test: a wait that nothing completes gives up after `cycles`, sets *fault.
+cudaError_t launch_wait_selftest(int* fault, long long cycles, cudaStream_t s);
+
 // Non-finite grad check: sets *flag = 1 if any grad (times g_unscale) is inf or NaN.
 template <bool GBF16, int CAP>
 cudaError_t launch_check_grads(const LaunchArgs<CAP>& a, int* flag, cudaStream_t s);

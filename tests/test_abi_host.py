@@ -164,3 +164,7 @@ def test_step_from_host_validation(psa):
     assert f(2, B(lst), P, P, bad, P, P, P, 1, B(hp), B(q), 4, None, None, None) == psa.ERR_MISALIGNED
     empty = psa._List(0, 0, nums, P, P, 1.0, 0, None, 0)
     assert f(2, B(empty), None, None, None, None, None, None, 1, B(hp), B(q), 4, None, None, None) == psa.OK
+
+
+def test_selftest_and_fault_validation(psa):
+    assert psa.cdll().psadam_selftest_bounded_wait(-1, None) == psa.ERR_INVALID_ARG

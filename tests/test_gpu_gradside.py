@@ -169,3 +169,20 @@ def test_mixed_precision_flow_skips_only_the_bad_step(psa):
     for i in range(len(SIZES)):
         got = [params[i].cpu().numpy(), *device_state_to_host(mode, state, i)]
         assert exact_fraction(mode, got, [p_host[i], *ostate[i]]) == 1.0
+
+
+def test_bounded_wait_reports_through_the_fault_word(psa):
+    """A kernel wait that nothing completes gives up after its cycle limit and sets the
+    library's fault word; psadam_device_fault reads it once and clears it. Steps leave it 0."""
+    assert psa.device_fault() == 0
+    lib = psa.cdll()
+    assert lib.psadam_selftest_bounded_wait(1 << 20, None) == psa.OK
+    torch.cuda.synchronize()
+    assert psa.device_fault() == 1
+    assert psa.device_fault() == 0
+    # a real step afterwards runs normally and reports nothing
+    params = [torch.randn(5000, device=DEV) * 0.02]
+    state = psa.zeros_state(params, "q8")
+    psa.adam_step_q8(params, [torch.randn(5000, device=DEV) * 1e-3], *state, 1)
+    torch.cuda.synchronize()
+    assert psa.device_fault() == 0
