@@ -216,7 +216,7 @@ def run_ours(args, rank: int, world: int, dist):
         kw.update(over)
         if args.zero_grads:
             kw.update(zero_grads=True)
-        launches_per_step = -(-len([n for n in sizes if n > 0]) // (8 if len(sizes) <= 8 else 440))
+        launches_per_step = launches_per_call(sizes)
         # one marshalled plan per grad set: a step is then a single C call
         plans = [psa.StepPlan(mode, params, grads[s], state, **kw) for s in range(n_sets)]
         t = 0
@@ -261,11 +261,53 @@ def run_ours(args, rank: int, world: int, dist):
         # ---- end to end through the public API with host buffers
         if spec == args.modes[0]:
             results[spec]["e2e"] = run_e2e(args, psa, torch, dev, stream, w, params, state, kw, t, flush, dist, world)
-            results[spec]["launches"] += launches_per_step * args.steps
+            results[spec]["launches"] += from_host_launches(sizes, args.e2e_chunks, bs) * args.steps
         del plans, params, state
         torch.cuda.empty_cache()
     clk = clocks.stop()
     return results, clk
+
+
+def launches_per_call(sizes) -> int:
+    """Kernel launches of one step call over a list: one per at most 8 tensors for lists of
+    up to 8, else one per at most 440 (empty tensors take no slot)."""
+    live = [n for n in sizes if n > 0]
+    if not live:
+        return 0
+    return -(-len(live) // (8 if len(live) <= 8 else 440))
+
+
+def from_host_launches(sizes, n_chunks: int, block_size: int) -> int:
+    """Launches of one psadam_step_from_host call: the library's chunking (whole tensors in
+    order; a tensor that does not fit the current chunk cut at a multiple of `unit` elements,
+    4 blocks rounded up to a multiple of 16), then launches_per_call for each chunk."""
+    live = [n for n in sizes if n > 0]
+    if not live:
+        return 0
+    if n_chunks <= 1:
+        return launches_per_call(live)
+    unit = 4 * block_size
+    while unit % 16:
+        unit *= 2
+    target = max(unit, -(-(sum(live) // n_chunks) // unit) * unit)
+    chunks, cur, size = [], [], 0
+    for n in live:
+        lo = 0
+        while lo < n:
+            hi = n if n - lo <= target - size else lo + (target - size) // unit * unit
+            if hi <= lo:
+                chunks.append(cur)
+                cur, size = [], 0
+                continue
+            cur.append(hi - lo)
+            size += hi - lo
+            lo = hi
+            if size >= target or lo < n:
+                chunks.append(cur)
+                cur, size = [], 0
+    if cur:
+        chunks.append(cur)
+    return sum(launches_per_call(c) for c in chunks if c)
 
 
 def run_e2e(args, psa, torch, dev, stream, w, params, state, kw, t, flush, dist, world):
