@@ -49,7 +49,8 @@ STATE_BYTES = {"fp32": (4, 4), "bf16m": (2, 2), "q8": (1, 1), "q8v": (4, 1)}   #
 
 
 def parse_mode(spec: str):
-    """"q8/bs256/p99" -> ("q8", {"block_size": 256, "percentile": 99.0})."""
+    """"q8/bs256/p99/sr" -> ("q8", {"block_size": 256, "percentile": 99.0,
+    "stochastic_rounding": True}); "approx" asks for the approximate update."""
     base, *opts = spec.split("/")
     if base not in STATE_BYTES:
         raise SystemExit(f"unknown moment mode {base!r}")
@@ -61,6 +62,8 @@ def parse_mode(spec: str):
             over["block_size"] = int(o[2:])
         elif o.startswith("p") and base in ("q8", "q8v"):
             over["percentile"] = float(o[1:])
+        elif o == "sr" and base in ("q8", "q8v"):
+            over["stochastic_rounding"] = True
         else:
             raise SystemExit(f"bad mode option {o!r} in {spec!r}")
     return base, over
@@ -381,7 +384,8 @@ def oracle_sample_rate(w: workloads.Workload, spec: str, budget_s: float):
     if w.grad_dtype == "bf16":
         g = (g.view(np.uint32) >> 16).astype(np.uint16)
     hp = oracle.HParams(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay)
-    q8 = oracle.Q8Opts(w.stochastic_rounding, w.seed, over.get("percentile", w.percentile), block_size=bs)
+    q8 = oracle.Q8Opts(over.get("stochastic_rounding", w.stochastic_rounding), w.seed,
+                       over.get("percentile", w.percentile), block_size=bs)
     done, t, t0 = 0, 0, time.perf_counter()
     while True:
         t += 1
