@@ -280,6 +280,9 @@ def launches_per_call(sizes) -> int:
     return -(-len(live) // (8 if len(live) <= 8 else 440))
 
 
+MAX_CUT = 4 * (2**31 - 1)  # last element offset at which psadam_step_from_host may cut a tensor
+
+
 def from_host_launches(sizes, n_chunks: int, block_size: int) -> int:
     """Launches of one psadam_step_from_host call: the library's chunking (whole tensors in
     order; a tensor that does not fit the current chunk cut at a multiple of `unit` elements,
@@ -298,6 +301,8 @@ def from_host_launches(sizes, n_chunks: int, block_size: int) -> int:
         lo = 0
         while lo < n:
             hi = n if n - lo <= target - size else lo + (target - size) // unit * unit
+            if hi < n and hi > MAX_CUT:  # the library cuts no tensor past 4 * INT_MAX elements
+                hi = n
             if hi <= lo:
                 chunks.append(cur)
                 cur, size = [], 0

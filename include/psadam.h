@@ -166,7 +166,8 @@ int adam_step_q8v(const psadam_list* list, float* const* m, uint8_t* const* v_co
  * m_scale, v_scale the arrays the matching adam_step_* call takes (NULL where that call has
  * none; q8 options only for modes 2 and 3). With stream_in and stream_out (two streams other
  * than `stream`) the list is cut into about n_chunks chunks (whole tensors; a larger tensor
- * at multiples of 4 quantization blocks and 16 elements) whose uploads (stream_in), steps
+ * at multiples of 4 quantization blocks and 16 elements, never past its first 4*INT_MAX
+ * elements: the rest of a larger tensor is one slice) whose uploads (stream_in), steps
  * (stream) and downloads (stream_out) overlap; NULL streams run it all on `stream`. Either
  * way the results are bit for bit those of one adam_step_* call over the whole list (a
  * slice keeps its tensor's element offsets and list position for stochastic rounding), and

@@ -375,6 +375,11 @@ int cuda_fail(cudaError_t e) {
   return PSADAM_ERR_CUDA;
 }
 
+// A slice's first element / 4 reaches the kernels as an int (the stochastic-rounding counter
+// offset, TensorRef::grp_off), so no cut lies past 4 * INT_MAX elements of a tensor: the rest
+// of a larger tensor stays in one slice.
+constexpr long long kMaxCut = 4LL * INT_MAX;
+
 // The list cut into chunks of about total/n_chunks elements: whole tensors in order, a tensor
 // that does not fit the current chunk cut at a multiple of `unit` elements from its start.
 std::vector<std::vector<Entry>> make_chunks(const std::vector<Entry>& es, int n_chunks, long long unit, int mode,
@@ -391,6 +396,7 @@ std::vector<std::vector<Entry>> make_chunks(const std::vector<Entry>& es, int n_
     long long lo = 0;
     while (lo < e.numel) {
       long long hi = e.numel - lo <= target - size ? e.numel : lo + (target - size) / unit * unit;
+      if (hi < e.numel && e.elem_off + hi > kMaxCut) hi = e.numel;
       if (hi <= lo) {  // not even one unit fits: close the chunk first
         chunks.emplace_back();
         size = 0;
