@@ -113,8 +113,10 @@ def test_step_ragged_list(psa, mode, grad_dtype, approx):
 Q8_CASES = {
     "rne_absmax": Q8Opts(False, 42, 100.0),
     "sr_absmax": Q8Opts(True, 42, 100.0),
-    "rne_p99.9": Q8Opts(False, 42, 99.9),   # rank 3 of a full block (K = 4 kernel)
+    "rne_p99.9": Q8Opts(False, 42, 99.9),   # rank 3 of a full block
     "sr_p99.9": Q8Opts(True, 7, 99.9),
+    "rne_p99.95": Q8Opts(False, 42, 99.95),  # rank 2 of a full block
+    "rne_p99.85": Q8Opts(False, 42, 99.85),  # rank 4: the largest rank of the 2048-block kernels
     "rne_p99.5": Q8Opts(False, 42, 99.5),   # rank 11: the general kernel's radix select
     "rne_static": Q8Opts(False, 42, 100.0, True),  # scales kept after the first step
     "sr_static_p99.9": Q8Opts(True, 5, 99.9, True),
@@ -234,8 +236,9 @@ def test_long_list_spans_several_launches(psa):
 @pytest.mark.parametrize("case", sorted(Q8_CASES))
 def test_quantize_only_is_bit_exact(psa, case):
     q8 = Q8_CASES[case]
-    sizes = RAGGED + [2048 * 5]
+    sizes = RAGGED + [2048 * 5, 2048 * 4]
     ms, vs = [], []
+    rng = np.random.default_rng(8)
     for i, n in enumerate(sizes):
         m, v = workloads.random_moments_np(n, seed=20 + i)
         if n == 2048 * 5:
@@ -243,6 +246,20 @@ def test_quantize_only_is_bit_exact(psa, case):
             v[2048:4096] = 0.0
             m[:2048] = 3e-4     # a constant block
             v[4096] = 1.0       # a single outlier
+        if n == 2048 * 4:
+            # block 0: the block's 8 largest all held by one thread (elements t*4 + i and
+            # 1024 + t*4 + i of thread t); block 1: the maximum 6 times over; block 2: small
+            # integers (ties everywhere); block 3: two non-zeros
+            for j, e in enumerate([37 * 4 + i for i in range(4)] + [1024 + 37 * 4 + i for i in range(4)]):
+                m[e] = (-1) ** j * (0.01 + j * 1e-3)
+                v[e] = 0.01 + j * 1e-3
+            top = rng.choice(2048, 6, replace=False) + 2048
+            m[top], v[top] = -0.02, 0.02
+            m[4096:6144] = rng.integers(-3, 4, 2048) * 1e-3
+            v[4096:6144] = rng.integers(0, 4, 2048) * 1e-6
+            m[6144:], v[6144:] = 0.0, 0.0
+            m[6144 + 5], v[6144 + 5] = 1e-3, 1e-6
+            m[6144 + 1500], v[6144 + 1500] = -2e-3, 3e-6
         ms.append(m)
         vs.append(v)
     dm, dv = _to_dev(ms), _to_dev(vs)
