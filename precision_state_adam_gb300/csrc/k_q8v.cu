@@ -3,7 +3,7 @@
 
 namespace psadam {
 #define PSADAM_INST(GB, SR, K, CAP) template cudaError_t launch_step<kModeQ8V, GB, SR, K, CAP>(const LaunchArgs<CAP>&, cudaStream_t);
-#define PSADAM_INST_K(GB, SR, CAP) PSADAM_INST(GB, SR, 1, CAP) PSADAM_INST(GB, SR, 4, CAP)
+#define PSADAM_INST_K(GB, SR, CAP) PSADAM_INST(GB, SR, 1, CAP) PSADAM_INST(GB, SR, 3, CAP) PSADAM_INST(GB, SR, 4, CAP)
 PSADAM_INST_K(false, false, kCapSmall)
 PSADAM_INST_K(true, false, kCapSmall)
 PSADAM_INST_K(false, false, kCapLarge)

@@ -216,6 +216,7 @@ Launcher<CAP> pick_step(int mode, bool gb, bool sr, int K) {
   if (mode == kModeBF16) return gb ? PSADAM_STEP_FN(kModeBF16, true, false, 1, CAP) : PSADAM_STEP_FN(kModeBF16, false, false, 1, CAP);
 #define PSADAM_PICK_K(MODE, GB, SR)                                 \
   if (K == 1) return PSADAM_STEP_FN(MODE, GB, SR, 1, CAP);          \
+  if (K == 3) return PSADAM_STEP_FN(MODE, GB, SR, 3, CAP);          \
   return PSADAM_STEP_FN(MODE, GB, SR, 4, CAP);
 #define PSADAM_PICK_MODE(MODE)                                      \
   if (gb) {                                                         \
@@ -241,8 +242,8 @@ Launcher<CAP> pick_step_any(int mode, bool gb, bool sr) {
 
 template <int CAP>
 Launcher<CAP> pick_quantize(bool sr, int K) {
-  if (sr) return K == 1 ? &launch_quantize<true, 1, CAP> : &launch_quantize<true, 4, CAP>;
-  return K == 1 ? &launch_quantize<false, 1, CAP> : &launch_quantize<false, 4, CAP>;
+  if (sr) return K == 1 ? &launch_quantize<true, 1, CAP> : (K == 3 ? &launch_quantize<true, 3, CAP> : &launch_quantize<true, 4, CAP>);
+  return K == 1 ? &launch_quantize<false, 1, CAP> : (K == 3 ? &launch_quantize<false, 3, CAP> : &launch_quantize<false, 4, CAP>);
 }
 
 // Dispatch on list length: short lists use the small parameter block.

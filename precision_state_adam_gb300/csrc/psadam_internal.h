@@ -17,8 +17,8 @@ constexpr int kWarps = kThreads / 32;
 // long lists the largest block that stays under the 32,764-byte parameter limit.
 constexpr int kCapSmall = 8;
 constexpr int kCapLarge = 440;
-// Largest percentile rank k the 2048-block kernels select (their top-K merge network; for
-// higher ranks the general kernel's radix select measured faster).
+// Largest percentile rank k the 2048-block kernels select (per-lane sorted top-K lists and
+// warp extraction; for higher ranks the general kernel's radix select measured faster).
 constexpr int kMaxRank = 4;
 // Largest quantization block of the any-block-size kernels (its fp32 m', v' are staged in
 // shared memory: 128 KB for both moments).
@@ -75,8 +75,9 @@ struct LaunchArgs {
 };
 static_assert(sizeof(LaunchArgs<kCapLarge>) <= 32764, "kernel parameter block too large");
 
-// Rank templates: K = 1 (absmax) or 4 (k-th largest for k <= 4).
-constexpr int rank_template(int k) { return k <= 1 ? 1 : 4; }
+// Rank templates: K = 1 (absmax), 3 (k-th largest for k = 2, 3: percentile 99.9 on full
+// blocks) or 4 (k = 4).
+constexpr int rank_template(int k) { return k <= 1 ? 1 : (k <= 3 ? 3 : 4); }
 
 // Launchers, explicitly instantiated in the kernel translation units.
 template <int MODE, bool GBF16, bool SR, int K, int CAP>
