@@ -136,6 +136,11 @@ class ClockSampler:
             return
         self.thread = threading.Thread(target=self._read, daemon=True)
         self.thread.start()
+        # nvidia-smi takes a moment to start: wait for its first sample (at most 5 s) so the
+        # samples span the timed regions that follow
+        t0 = time.time()
+        while not self.rows and time.time() - t0 < 5.0 and self.proc.poll() is None:
+            time.sleep(0.02)
 
     def _read(self):
         for line in self.proc.stdout:
