@@ -20,7 +20,8 @@ value      = params updated per second over all ranks (Gparams/s), device-timed
 e2e        = the same through the public API with host buffers: each step copies its grads
              from pinned host memory and the updated params back, inside the timed span
 roofline   = algorithmic HBM bytes per launch / mean launch time vs MEASURED_PEAKS.json
-cpu_baseline = the CPU oracle (single thread) on a bounded sample of the workload
+cpu_baseline = the CPU oracle (single thread) on a bounded sample of the workload; its
+             all_cores entry: the same oracle on every host core, one sample per thread
 
 Under torchrun (N > 1) every rank runs its own shard of the same size on its own GPU
 (weak scaling, no collective in the step); the time is the max over ranks.
@@ -370,42 +371,76 @@ def run_e2e(args, psa, torch, dev, stream, w, params, state, kw, t, flush, dist,
 
 
 # ------------------------------------------------------------------ the CPU oracle as a baseline
-def oracle_sample_rate(w: workloads.Workload, spec: str, budget_s: float):
-    """Time the CPU oracle (as it is: plain scalar C, one thread) on whole 2048-element
-    blocks of the workload's first tensor, step after step, for about `budget_s` seconds."""
+def oracle_sample_rate(w: workloads.Workload, spec: str, budget_s: float, threads: int = 1):
+    """Time the CPU oracle (as it is: plain scalar C) on whole 2048-element blocks of the
+    workload's first tensor, step after step, for about `budget_s` seconds. With threads > 1
+    each thread steps its own copy of the sample (the oracle's C calls release the GIL) and
+    the rate is the params all threads updated per second."""
     import numpy as np
     import oracle
 
     mode, over = parse_mode(spec)
     bs = over.get("block_size", 2048)
     n = min(w.sizes[0], 256 * 2048)
-    rng = np.random.default_rng(0)
-    p = (rng.standard_normal(n) * 0.02).astype(np.float32)
-    if mode == "fp32":
-        st = [np.zeros(n, np.float32), np.zeros(n, np.float32)]
-    elif mode == "bf16m":
-        st = [np.zeros(n, np.uint16), np.zeros(n, np.uint16)]
-    elif mode == "q8v":
-        st = [np.zeros(n, np.float32), np.zeros(n, np.uint8), np.zeros(oracle.n_blocks(n, bs), np.float32)]
-    else:
-        nb = oracle.n_blocks(n, bs)
-        st = [np.zeros(n, np.int8), np.zeros(n, np.uint8), np.zeros(nb, np.float32), np.zeros(nb, np.float32)]
-    g = (rng.standard_normal(n) * w.grad_std).astype(np.float32)
-    if w.grad_dtype == "bf16":
-        g = (g.view(np.uint32) >> 16).astype(np.uint16)
+
+    def sample():
+        rng = np.random.default_rng(0)
+        p = (rng.standard_normal(n) * 0.02).astype(np.float32)
+        if mode == "fp32":
+            st = [np.zeros(n, np.float32), np.zeros(n, np.float32)]
+        elif mode == "bf16m":
+            st = [np.zeros(n, np.uint16), np.zeros(n, np.uint16)]
+        elif mode == "q8v":
+            st = [np.zeros(n, np.float32), np.zeros(n, np.uint8), np.zeros(oracle.n_blocks(n, bs), np.float32)]
+        else:
+            nb = oracle.n_blocks(n, bs)
+            st = [np.zeros(n, np.int8), np.zeros(n, np.uint8), np.zeros(nb, np.float32), np.zeros(nb, np.float32)]
+        g = (rng.standard_normal(n) * w.grad_std).astype(np.float32)
+        if w.grad_dtype == "bf16":
+            g = (g.view(np.uint32) >> 16).astype(np.uint16)
+        return p, g, st
+
     hp = oracle.HParams(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay)
     q8 = oracle.Q8Opts(over.get("stochastic_rounding", w.stochastic_rounding), w.seed,
                        over.get("percentile", w.percentile), block_size=bs)
-    done, t, t0 = 0, 0, time.perf_counter()
-    while True:
-        t += 1
-        oracle.step_list(mode, [p], [g], [st], t, hp, q8)
-        done += n
-        el = time.perf_counter() - t0
-        if el >= budget_s:
-            break
-    return done / el / 1e9, f"{t} steps over the first {n:,} params of the workload ({-(-n // bs)} blocks), " \
-                            f"{el:.1f} s, one thread"
+    samples = [sample() for _ in range(threads)]
+    steps = [0] * threads
+    start = threading.Barrier(threads)
+    t0 = [0.0]
+
+    def worker(i):
+        p, g, st = samples[i]
+        start.wait()
+        if i == 0:
+            t0[0] = time.perf_counter()
+        t, begin = 0, time.perf_counter()
+        while True:
+            t += 1
+            oracle.step_list(mode, [p], [g], [st], t, hp, q8)
+            if time.perf_counter() - begin >= budget_s:
+                break
+        steps[i] = t
+
+    if threads == 1:
+        worker(0)
+    else:
+        pool = [threading.Thread(target=worker, args=(i,)) for i in range(threads)]
+        for th in pool:
+            th.start()
+        for th in pool:
+            th.join()
+    el = time.perf_counter() - t0[0]
+    done = n * sum(steps)
+    who = "one thread" if threads == 1 else f"{threads} threads, each on its own copy"
+    return done / el / 1e9, f"{sum(steps)} steps over the first {n:,} params of the workload ({-(-n // bs)} blocks), " \
+                            f"{el:.1f} s, {who}"
+
+
+def host_threads() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
 
 
 def run_reference(args, rank, world):
@@ -451,6 +486,7 @@ def main():
     ap.add_argument("--e2e-chunks", type=int, default=8,
                     help="end-to-end leg: chunks whose copies overlap the step (1 = one stream, in series)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--cpu-seconds-all", type=float, default=6.0, help="oracle on every host core (0: skip)")
     ap.add_argument("--ref-step-seconds", type=float, default=3.0)
     args = ap.parse_args()
     w = workloads.WORKLOADS[args.workload]
@@ -496,6 +532,10 @@ def main():
         if world == 1 and not args.no_cpu_baseline:
             v, sample = oracle_sample_rate(w, head, args.cpu_seconds)
             cpu = {"value": round(v, 6), "unit": "Gparams/s", "cores": 1, "kind": "oracle", "sample": sample}
+            nt = host_threads()
+            if nt > 1 and args.cpu_seconds_all > 0:  # the oracle on every host core, each thread its own sample
+                va, sa = oracle_sample_rate(w, head, args.cpu_seconds_all, threads=nt)
+                cpu["all_cores"] = {"value": round(va, 6), "unit": "Gparams/s", "cores": nt, "sample": sa}
         # the captures are of the plain step; grad zeroing runs another kernel flavour
         traffic = None if args.zero_grads else ncu_traffic(w.name, head)
         line = {
