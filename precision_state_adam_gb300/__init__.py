@@ -138,6 +138,12 @@ def _stream_handle(stream, ts) -> int | None:
 
 
 def _check_layout(name: str, ts, dtype, like=None, numel_fn=None) -> None:
+    """Every tensor of ``ts``: ``dtype``, contiguous, on the CUDA device of its counterpart in
+    ``like`` (of ``ts[0]`` without one) and, with ``like``, one per tensor of ``like`` with the
+    element count ``numel_fn`` gives (the same count by default). The library reads as many
+    pointers from every table as the list has tensors, so a short table is refused here."""
+    if like is not None and len(ts) != len(like):
+        raise ValueError(f"{name}: {len(ts)} tensors for a list of {len(like)}")
     for i, t in enumerate(ts):
         if t.dtype != dtype:
             raise TypeError(f"{name}[{i}]: expected {dtype}, got {t.dtype}")
@@ -145,6 +151,9 @@ def _check_layout(name: str, ts, dtype, like=None, numel_fn=None) -> None:
             raise TypeError(f"{name}[{i}]: must be a CUDA tensor")
         if not t.is_contiguous():
             raise ValueError(f"{name}[{i}]: must be contiguous")
+        dev = like[i].device if like is not None else ts[0].device
+        if t.device != dev:
+            raise ValueError(f"{name}[{i}]: on {t.device}, expected {dev}")
         if like is not None:
             want = numel_fn(like[i].numel()) if numel_fn else like[i].numel()
             if t.numel() != want:

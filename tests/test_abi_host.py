@@ -7,6 +7,7 @@ import os
 import re
 
 import pytest
+import torch
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "psadam.h")
@@ -168,3 +169,18 @@ def test_step_from_host_validation(psa):
 
 def test_selftest_and_fault_validation(psa):
     assert psa.cdll().psadam_selftest_bounded_wait(-1, None) == psa.ERR_INVALID_ARG
+
+
+def test_binding_refuses_short_pointer_tables(psa):
+    # the library reads one pointer per list tensor from every table: a state list shorter
+    # than the param list is refused before any call (checked before the device checks, so
+    # CPU tensors show it)
+    a, b = torch.zeros(4), torch.zeros(8)
+    with pytest.raises(ValueError, match="1 tensors for a list of 2"):
+        psa._check_layout("m", [a], torch.float32, like=[a, b])
+    with pytest.raises(ValueError, match="tensors for a list of"):
+        psa._check_layout("m", [a, b, a], torch.float32, like=[a, b])
+    with pytest.raises(TypeError, match="must be a CUDA tensor"):
+        psa._check_layout("m", [a, b], torch.float32, like=[a, b])
+    with pytest.raises(TypeError, match="expected torch.float32"):
+        psa._check_layout("m", [a.double()], torch.float32)
