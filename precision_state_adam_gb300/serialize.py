@@ -106,24 +106,37 @@ def load_state(f: str | BinaryIO, device=None):
     version, hlen = struct.unpack("<II", data[8:16])
     if version != VERSION:
         raise StateFormatError(f"unsupported format version {version}")
-    header = json.loads(data[16:16 + hlen].decode())
-    mode = header["mode"]
-    bs = header.get("block_size")
+    if 16 + hlen > len(data) - 4:
+        raise StateFormatError("header runs past the end of the file")
+    try:
+        header = json.loads(data[16:16 + hlen].decode())
+        mode = header["mode"]
+        bs = header.get("block_size")
+        flags = (header["compress_both_moments"], header["has_v_quantized"])
+        numel, arrays = header["numel"], header["arrays"]
+        int(header["step"])
+    except (ValueError, UnicodeDecodeError, KeyError, TypeError, AttributeError) as e:
+        raise StateFormatError(f"unreadable header: {e}") from None
     if mode not in _LAYOUT or not isinstance(bs, int) or not 1 <= bs <= MAX_BLOCK:
         raise StateFormatError(f"unsupported mode / block size: {mode}, {bs}")
-    if header["compress_both_moments"] != (mode == "q8") or header["has_v_quantized"] != (mode in ("q8", "q8v")):
+    if flags != (mode == "q8", mode in ("q8", "q8v")):
         raise StateFormatError("flags disagree with the moment mode")
+    if not isinstance(numel, list) or not all(isinstance(n, int) and n >= 0 for n in numel):
+        raise StateFormatError("numel must be a list of non-negative integers")
     layout = _LAYOUT[mode]
+    if not isinstance(arrays, list) or len(arrays) != len(numel) * len(layout) or \
+            not all(isinstance(a, list) and len(a) == 3 for a in arrays):
+        raise StateFormatError(f"array list does not match {len(numel)} tensors of the {mode} layout")
     parts = [[] for _ in layout]
     off = 16 + hlen
-    it = iter(header["arrays"])
-    for i, n in enumerate(header["numel"]):
+    it = iter(arrays)
+    for i, n in enumerate(numel):
         for j, (name, dtype, kind) in enumerate(layout):
             aname, dname, count = next(it)
             if aname != f"{i}.{name}" or _NAME_DTYPE.get(dname) != dtype or count != _count(kind, n, bs):
                 raise StateFormatError(f"array {aname} does not match the {mode} layout")
             size = count * (2 if dtype == torch.bfloat16 else torch.empty(0, dtype=dtype).element_size())
-            raw = bytearray(data[off:off + size])
+            raw = bytearray(data[off:min(off + size, len(data) - 4)])  # never into the checksum
             if len(raw) != size:
                 raise StateFormatError("file is truncated")
             off += size

@@ -92,3 +92,41 @@ def test_round_trip_other_block_size(psa, mode):
             assert torch.equal(a, b)
     with pytest.raises(ValueError):  # scales sized for the default block
         psa.save_state(io.BytesIO(), mode, st, step=3)
+
+
+def _forge(header_bytes: bytes, body: bytes = b"") -> io.BytesIO:
+    import struct
+    import zlib
+    blob = b"PSADAMST" + struct.pack("<II", 1, len(header_bytes)) + header_bytes + body
+    return io.BytesIO(blob + struct.pack("<I", zlib.crc32(blob) & 0xFFFFFFFF))
+
+
+def test_malformed_headers_are_format_errors(psa):
+    # files whose checksum is right but whose header is not a valid state header
+    import json
+    good = {"mode": "fp32", "step": 1, "block_size": 2048, "compress_both_moments": False,
+            "has_v_quantized": False, "hparams": {}, "q8": {}, "numel": [2],
+            "arrays": [["0.m", "f32", 2], ["0.v", "f32", 2]]}
+    body = bytes(16)
+    mode, st, step, _ = psa.load_state(_forge(json.dumps(good).encode(), body))
+    assert mode == "fp32" and step == 1 and st[0][0].numel() == 2
+    cases = [
+        b"not json",
+        b"[1, 2, 3]",                                         # not an object
+        json.dumps({k: v for k, v in good.items() if k != "numel"}).encode(),
+        json.dumps({**good, "numel": [-4]}).encode(),
+        json.dumps({**good, "numel": "2"}).encode(),
+        json.dumps({**good, "arrays": [["0.m", "f32", 2]]}).encode(),        # one array short
+        json.dumps({**good, "arrays": [["0.m", "f32", 2], ["0.v", "f32"]]}).encode(),
+        json.dumps({**good, "mode": "q4"}).encode(),
+        json.dumps({**good, "block_size": 0}).encode(),
+        json.dumps({**good, "has_v_quantized": True}).encode(),
+        json.dumps({**good, "step": "x"}).encode(),
+    ]
+    for hb in cases:
+        with pytest.raises(psa.StateFormatError):
+            psa.load_state(_forge(hb, body))
+    with pytest.raises(psa.StateFormatError, match="truncated"):
+        psa.load_state(_forge(json.dumps(good).encode(), body[:12]))
+    with pytest.raises(psa.StateFormatError, match="trailing"):
+        psa.load_state(_forge(json.dumps(good).encode(), body + b"\0"))
