@@ -31,6 +31,7 @@ from __future__ import annotations
 import argparse
 import glob
 import hashlib
+import io
 import json
 import os
 import statistics
@@ -129,12 +130,28 @@ class ClockSampler:
         self.thread = None
 
     def start(self):
+        # nvidia-smi's output goes to a pseudo-terminal: into a pipe it is block-buffered and
+        # its samples would only arrive when it exits
+        import pty
+        try:
+            master, slave = pty.openpty()
+        except OSError:
+            master = slave = None
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                                          "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                                          "-lms", "100"], stdout=slave if slave is not None else subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, stdin=subprocess.DEVNULL)
         except OSError:
             self.proc = None
+            for fd in (master, slave):
+                if fd is not None:
+                    os.close(fd)
             return
+        if slave is not None:
+            os.close(slave)
+            self.stream = os.fdopen(master, "r", errors="replace")
+        else:
+            self.stream = io.TextIOWrapper(self.proc.stdout, errors="replace")
         self.thread = threading.Thread(target=self._read, daemon=True)
         self.thread.start()
         # nvidia-smi takes a moment to start: wait for its first sample (at most 5 s) so the
@@ -144,10 +161,13 @@ class ClockSampler:
             time.sleep(0.02)
 
     def _read(self):
-        for line in self.proc.stdout:
-            parts = [x.strip() for x in line.split(",")]
-            if len(parts) >= 8:
-                self.rows.append(parts)
+        try:
+            for line in self.stream:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 8:
+                    self.rows.append(parts)
+        except OSError:  # the terminal's other end closed (EIO)
+            pass
 
     def stop(self):
         if self.proc is None:
@@ -158,6 +178,10 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.thread.join(timeout=5)
+        try:
+            self.stream.close()
+        except OSError:
+            pass
         rows = [r for r in self.rows if self.uuid is None or self.uuid in r[0]] or self.rows
         if not rows:
             return None

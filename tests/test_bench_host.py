@@ -64,3 +64,35 @@ def test_workload_sizes_match_the_stated_counts():
     assert len(w["gpt_1p3b"].sizes) == 292 and sum(w["gpt_1p3b"].sizes) == 1_315_819_520
     assert w["flat_16m"].sizes == [16_777_216]
     assert w["flat_1g_heavy"].sizes == [1 << 30]
+
+
+def test_clock_sampler_sees_samples_while_it_runs(tmp_path, monkeypatch):
+    # a stand-in for nvidia-smi that, like it, buffers its output fully unless it writes to a
+    # terminal: the sampler must see its lines while it runs, not only when it exits
+    import os
+    import sys
+    import time
+    fake = tmp_path / "nvidia-smi"
+    fake.write_text(
+        f"#!{sys.executable}\n"
+        "import time\n"
+        "for i in range(200):\n"
+        "    print('GPU-1, %d, 2070, 500.0, Not Active, Not Active, Not Active, %s'\n"
+        "          % (2070 - i % 2, 'Active' if i == 3 else 'Not Active'))\n"
+        "    time.sleep(0.05)\n")
+    fake.chmod(0o755)
+    monkeypatch.setenv("PATH", f"{tmp_path}{os.pathsep}{os.environ['PATH']}")
+    c = bench.ClockSampler("GPU-1")
+    c.start()
+    time.sleep(1.0)
+    got = c.stop()
+    assert got is not None and got["samples"] >= 5
+    assert got["sm_max_mhz"] == 2070.0 and 2069.0 <= got["sm_mhz"] <= 2070.0
+    assert got["reasons"] == ["sw_power_cap"]
+
+
+def test_clock_sampler_without_nvidia_smi(tmp_path, monkeypatch):
+    monkeypatch.setenv("PATH", str(tmp_path))
+    c = bench.ClockSampler(None)
+    c.start()
+    assert c.stop() is None
