@@ -102,7 +102,8 @@ typedef struct {
                                     UNSUPPORTED above); PR #814's default is 2048 */
     int32_t stochastic_rounding; /* 0: round to nearest even; 1: Philox stochastic rounding */
     uint64_t seed;               /* Philox key (stochastic rounding only) */
-    float percentile;            /* (0, 100]; 100 = absmax */
+    float percentile;            /* (0, 100]; 100 = absmax. PR #814's options list
+                                    defaults to 99.9 (3rd largest of a full block) */
     int32_t static_scales;       /* 0: scales recomputed every step (PR #814's default
                                     UseDynamicQuantization = true). 1: a block keeps its scale
                                     once it is nonzero (set by its first quantization); values

@@ -240,7 +240,12 @@ def adam_step_q8(params, grads, m_code, v_code, m_scale, v_scale, step: int, lr:
                  zero_grads: bool = False, skip_flag=None, static_scales: bool = False, approx_update: bool = False,
                  stream=None) -> None:
     """One AdamW step with 8-bit block-wise moments (int8 m codes, uint8 v codes, fp32
-    per-block scales), dequantize-update-requantize in one pass, in place."""
+    per-block scales), dequantize-update-requantize in one pass, in place.
+
+    Defaults follow the 8-bit Adam PR's options list (block 2048, scales recomputed every
+    step, round to nearest, seed 42) except the percentile: the options list defaults to
+    99.9 (the block's 3rd-largest magnitude sets the scale); here the default is absmax
+    (percentile 100), the faster kernel. Pass ``percentile=99.9`` for the listed default."""
     lst, keep = _list(params, grads, grad_unscale, zero_grads, skip_flag, approx_update=approx_update)
     _check_layout("m_code", m_code, torch.int8, params)
     _check_layout("v_code", v_code, torch.uint8, params)
@@ -260,7 +265,8 @@ def adam_step_q8v(params, grads, m, v_code, v_scale, step: int, lr: float = 1e-3
                   zero_grads: bool = False, skip_flag=None, static_scales: bool = False, approx_update: bool = False,
                  stream=None) -> None:
     """One AdamW step with an fp32 first moment and an 8-bit block-wise second moment
-    (uint8 v codes, fp32 per-block scales), in place."""
+    (uint8 v codes, fp32 per-block scales), in place. Defaults as :func:`adam_step_q8`
+    (absmax; the options list's percentile default is 99.9)."""
     lst, keep = _list(params, grads, grad_unscale, zero_grads, skip_flag, approx_update=approx_update)
     _check_layout("m", m, torch.float32, params)
     _check_layout("v_code", v_code, torch.uint8, params)
