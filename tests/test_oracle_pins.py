@@ -403,6 +403,86 @@ def test_stochastic_rounding_brackets_and_is_unbiased():
         assert (oracle.quantize_block(x, True, **other)[0] != base).any()
 
 
+def _sr_expected_codes(x: np.ndarray, s: np.float32, seed: int, step: int, list_idx: int, moment: int,
+                       elem0: int, qmin: int, qmax: int) -> np.ndarray:
+    """clamp(floor(fl(fl(x / s) + u))) per element, with u drawn here straight from the Philox
+    primitive (pinned to Triton's implementation): element e of list tensor i takes word e % 4
+    of Philox4x32-10(counter = (e // 4 low, e // 4 high, step, 2 i + moment), key = seed) and
+    u = (word >> 8) * 2^-24. e is the element's index within its whole tensor."""
+    e = elem0 + np.arange(x.size, dtype=np.int64)
+    grp = (e // 4).astype(np.uint64)
+    ctr = np.stack([(grp & 0xFFFFFFFF).astype(np.uint32), (grp >> np.uint64(32)).astype(np.uint32),
+                    np.full(x.size, step, np.uint32), np.full(x.size, 2 * list_idx + moment, np.uint32)], axis=1)
+    key = np.array([seed & 0xFFFFFFFF, seed >> 32], np.uint32)
+    words = oracle.philox4x32_10(ctr, key)[np.arange(x.size), e % 4]
+    u = ((words >> np.uint32(8)).astype(np.float64) * 2.0 ** -24).astype(F32)
+    if s == 0:
+        return np.zeros(x.size, np.int64)
+    ratio = (x.astype(F32) / F32(s)).astype(F32)          # one IEEE fp32 division
+    r = np.floor((ratio + u).astype(F32)).astype(np.int64)  # one fp32 addition, then floor
+    return np.clip(r, qmin, qmax)
+
+
+@pytest.mark.parametrize("mode", ["q8", "q8v"])
+def test_sr_stream_keying_inside_the_step(mode):
+    """The stochastic-rounding draw of every element inside a list step: element j of block b
+    of list tensor i uses the stream position e = b*B + j within its whole tensor and list
+    index i (PR #814 summary: stochastic rounding; the C# Random(42) replaced by a counter
+    stream keyed by seed, step and index). The expected codes are built here from m', v' of
+    the dequantize -> fp32 step decomposition and the Philox primitive alone, so dropping the
+    block offset or keying by the wrong list index fails this test."""
+    hp = HParams(lr=1e-3, weight_decay=0.01)
+    seed = 0x1234_5678_9ABC_DEF1  # high key word in use
+    sizes = [3000, 3 * 2048 + 77, 4 * 2048]  # list tensors 1 and 2: >= 3 blocks, a ragged tail
+    q8 = Q8Opts(stochastic_rounding=True, seed=seed, percentile=100.0)
+    params = [(_fresh(n, seed=40 + i)[0]) for i, n in enumerate(sizes)]
+    state = []
+    for n in sizes:
+        nb = oracle.n_blocks(n)
+        if mode == "q8":
+            state.append((np.zeros(n, np.int8), np.zeros(n, np.uint8), np.zeros(nb, F32), np.zeros(nb, F32)))
+        else:
+            state.append((np.zeros(n, F32), np.zeros(n, np.uint8), np.zeros(nb, F32)))
+    for t in (1, 2, 3):
+        grads = workloads.grads_np(sizes, t, 1e-2, seed=41)
+        # m', v' of this step: dequantize the state, then the fp32 step on copies
+        mv_new = []
+        for i, n in enumerate(sizes):
+            st = state[i]
+            if mode == "q8":
+                m0, v0 = oracle.dequantize(st[0], st[1], st[2], st[3])
+            else:
+                m0 = st[0].copy()
+                v0 = oracle.dequantize(np.zeros(n, np.int8), st[1], np.zeros_like(st[2]), st[2])[1]
+            pf = params[i].copy()
+            oracle.step_fp32(pf, grads[i], m0, v0, t, hp)
+            mv_new.append((m0, v0))
+        oracle.step_list(mode, params, grads, state, t, hp, q8)
+        checked = 0
+        for i, n in enumerate(sizes):
+            m1, v1 = mv_new[i]
+            st = state[i]
+            for b in range(oracle.n_blocks(n)):
+                lo, hi = b * 2048, min(n, (b + 1) * 2048)
+                chans = [(v1[lo:hi], st[1][lo:hi], (st[3] if mode == "q8" else st[2])[b], 1, 0, 255)]
+                if mode == "q8":
+                    chans.append((m1[lo:hi], st[0][lo:hi], st[2][b], 0, -127, 127))
+                for x, codes, s, moment, qmin, qmax in chans:
+                    # absmax scale: one fp32 division of the block maximum by the code range
+                    assert s == F32(F32(np.max(np.abs(x))) / F32(qmax))
+                    want = _sr_expected_codes(x, s, seed, t, i, moment, lo, qmin, qmax)
+                    np.testing.assert_array_equal(codes.astype(np.int64), want,
+                                                  err_msg=f"{mode} step {t} tensor {i} block {b} moment {moment}")
+                    checked += x.size
+        assert checked >= sum(sizes)
+    # the same block contents keyed by another list index or block offset give other codes
+    x = mv_new[1][1][2048:4096]
+    s = F32(F32(np.max(x)) / F32(255))
+    base = _sr_expected_codes(x, s, seed, 3, 1, 1, 2048, 0, 255)
+    assert (base != _sr_expected_codes(x, s, seed, 3, 0, 1, 2048, 0, 255)).any()
+    assert (base != _sr_expected_codes(x, s, seed, 3, 1, 1, 0, 0, 255)).any()
+
+
 def test_q8_step_uses_unquantized_moments_and_stores_their_codes():
     """From zero state the q8 step's params equal the fp32 step's bit for bit (the update
     reads m', v' before Quantize(m), Quantize(v)), and the stored codes are m', v'
