@@ -131,8 +131,10 @@ typedef struct {
                                     parameter update (see above); 0 = IEEE-exact */
 } psadam_list;
 
-/* One AdamW step with fp32 moments. m, v: host [n_tensors] of device float[numel],
- * updated in place. Fresh state is all zeros. */
+/* One AdamW step with fp32 moments (PR #1745, "The real fix": the fused Adam/AdamW kernel
+ * configured by (lr, beta1, beta2, eps, weight decay), fp32 moments being its default before
+ * the bf16 option). m, v: host [n_tensors] of device float[numel], updated in place. Fresh
+ * state is all zeros. */
 int adam_step_fp32(const psadam_list* list, float* const* m, float* const* v, int64_t step,
                    const psadam_hparams* hp, void* stream);
 
@@ -210,12 +212,17 @@ size_t psadam_state_bytes(int32_t mode, int64_t numel, int32_t block_size);
 
 /* 1 if a kernel of the library gave up a bounded wait on its own asynchronous copies since
  * the last call (its results are then not to be trusted), 0 if not, -1 if the device could
- * not be queried; reading clears it. Synchronises with the device. */
+ * not be queried. The call first waits for all work on the current device (every stream,
+ * cudaDeviceSynchronize), then takes the word and clears it in one atomic exchange on the
+ * legacy default stream, so a fault is never lost between the read and the clear. A CTA
+ * gives up as a whole (its threads agree at a barrier) and stores nothing of the block it was
+ * waiting for; blocks it finished before keep their results. */
 int32_t psadam_device_fault(void);
 
 /* Self-test of the failure path above: one thread waits on a barrier that nothing completes,
  * gives up after `cycles` SM cycles and sets the fault word (so the next
- * psadam_device_fault() returns 1). It never faults or hangs the device. */
+ * psadam_device_fault() returns 1). It never faults or hangs the device. cycles must lie in
+ * [0, 2^31], the step kernels' own limit (PSADAM_ERR_INVALID_ARG otherwise). */
 int psadam_selftest_bounded_wait(int64_t cycles, void* stream);
 
 /* Static, human-readable name of a psadam_status value. */

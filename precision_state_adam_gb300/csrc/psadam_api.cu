@@ -16,26 +16,27 @@ using namespace psadam;
 // Set to 1 by a kernel whose bounded wait gave up (read and cleared by psadam_device_fault).
 // A module variable: the library still allocates no device memory.
 __device__ int g_psadam_fault = 0;
+// Where psadam_device_fault's one-thread kernel leaves the value it took out of g_psadam_fault.
+__device__ int g_psadam_fault_taken = 0;
+
+// Read and clear the fault word in one atomic exchange, so a fault set meanwhile is either
+// taken now or left for the next read.
+__global__ void psadam_take_fault_kernel() { g_psadam_fault_taken = atomicExch(&g_psadam_fault, 0); }
 
 namespace {
 
 thread_local int32_t g_last_cuda_error = 0;
 
-// Device address of g_psadam_fault on the current device (looked up once per device).
+// Device address of g_psadam_fault in the current context. Looked up on every call (no cache,
+// so a context made anew after cudaDeviceReset gets its own address).
 int* fault_word() {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
-  constexpr int kMaxDev = 64;
-  static std::atomic<int*> cache[kMaxDev];
-  if (dev < kMaxDev) {
-    int* p = cache[dev].load(std::memory_order_relaxed);
-    if (p) return p;
-  }
   void* p = nullptr;
   if (cudaGetSymbolAddress(&p, g_psadam_fault) != cudaSuccess) return nullptr;
-  if (dev < kMaxDev) cache[dev].store(static_cast<int*>(p), std::memory_order_relaxed);
   return static_cast<int*>(p);
 }
+
+// The step kernels' own limit on a bounded wait, in SM cycles (about a second).
+constexpr long long kMaxWaitCycles = 1LL << 31;
 
 // Largest tensor whose block count fits a grid dimension.
 constexpr long long kMaxNumel = (long long)INT_MAX * kBlock;
@@ -623,7 +624,7 @@ size_t psadam_state_bytes(int32_t mode, int64_t numel, int32_t block_size) {
 }
 
 int psadam_selftest_bounded_wait(int64_t cycles, void* stream) {
-  if (cycles < 0) return PSADAM_ERR_INVALID_ARG;
+  if (cycles < 0 || cycles > kMaxWaitCycles) return PSADAM_ERR_INVALID_ARG;
   int* fault = fault_word();
   if (fault == nullptr) return PSADAM_ERR_CUDA;
   const cudaError_t e = launch_wait_selftest(fault, cycles, static_cast<cudaStream_t>(stream));
@@ -631,13 +632,14 @@ int psadam_selftest_bounded_wait(int64_t cycles, void* stream) {
 }
 
 int32_t psadam_device_fault(void) {
+  // every stream of the device, non-blocking ones included, has finished what it was given
+  if (cudaDeviceSynchronize() != cudaSuccess) return -1;
+  psadam_take_fault_kernel<<<1, 1>>>();
+  if (cudaGetLastError() != cudaSuccess) return -1;
   int v = 0;
-  if (cudaMemcpyFromSymbol(&v, g_psadam_fault, sizeof v) != cudaSuccess) return -1;
-  if (v != 0) {
-    const int zero = 0;
-    if (cudaMemcpyToSymbol(g_psadam_fault, &zero, sizeof zero) != cudaSuccess) return -1;
-  }
-  return v;
+  // ordered after the kernel on the legacy default stream
+  if (cudaMemcpyFromSymbol(&v, g_psadam_fault_taken, sizeof v) != cudaSuccess) return -1;
+  return v != 0 ? 1 : 0;
 }
 
 const char* psadam_status_string(int32_t status) {

@@ -168,7 +168,11 @@ def test_step_from_host_validation(psa):
 
 
 def test_selftest_and_fault_validation(psa):
-    assert psa.cdll().psadam_selftest_bounded_wait(-1, None) == psa.ERR_INVALID_ARG
+    lib = psa.cdll()
+    assert lib.psadam_selftest_bounded_wait(-1, None) == psa.ERR_INVALID_ARG
+    # no wait longer than the step kernels' own limit (2^31 SM cycles, about a second)
+    assert lib.psadam_selftest_bounded_wait((1 << 31) + 1, None) == psa.ERR_INVALID_ARG
+    assert lib.psadam_selftest_bounded_wait(2 ** 62, None) == psa.ERR_INVALID_ARG
 
 
 def test_binding_refuses_short_pointer_tables(psa):

@@ -96,3 +96,25 @@ def test_clock_sampler_without_nvidia_smi(tmp_path, monkeypatch):
     c = bench.ClockSampler(None)
     c.start()
     assert c.stop() is None
+
+
+def test_both_arms_report_the_same_config(monkeypatch, capsys):
+    """The reference arm (the CPU oracle) prints the very `config` dict the GPU arm prints for
+    the same workload and mode, so the two lines describe one workload."""
+    monkeypatch.setattr(bench, "oracle_sample_rate", lambda w, spec, budget, threads=1: (1e-3, "stub sample"))
+    monkeypatch.setattr("sys.argv", ["bench.py", "--impl", "reference", "--steps", "2", "--warmup", "3"])
+    bench.main()
+    import json
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    w = workloads.WORKLOADS["gpt_1p3b"]
+    assert line["impl"] == "reference"
+    assert line["config"] == bench.workload_config(w, "q8", False, 2, 3)
+    assert line["config"]["workload"] == "gpt_1p3b" and line["config"]["params"] == 1_315_819_520
+
+
+def test_grad_sets_stay_within_budget():
+    for name, w in workloads.WORKLOADS.items():
+        n = bench.n_grad_sets(w, 20, 5)
+        per = sum(w.sizes) * (4 if w.grad_dtype == "f32" else 2)
+        assert 2 <= n <= 8
+        assert n == 2 or n * per <= bench.GRAD_SET_BUDGET, name
