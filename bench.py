@@ -247,7 +247,7 @@ def bench_workload(args, w: workloads.Workload, modes, rank: int, world: int, di
     for spec in modes:
         mode, over = parse_mode(spec)
         bs = over.get("block_size", 2048)
-        params = workloads.init_params_torch(w.specs, dev, seed=workloads.DEFAULT_SEED + rank)
+        params = workloads.init_params_torch(w.specs, dev, seed=workloads.DEFAULT_SEED + rank, flat=True)
         state = psa.zeros_state(params, mode, bs)
         kw = dict(lr=w.lr, beta1=w.beta1, beta2=w.beta2, eps=w.eps, weight_decay=w.weight_decay)
         if mode in ("q8", "q8v"):
@@ -411,13 +411,18 @@ def run_e2e(args, psa, torch, dev, stream, w, spec, params, state, kw, t, flush,
     sizes = w.sizes
     mode, over = parse_mode(spec)
     gdt = torch.float32 if w.grad_dtype == "f32" else torch.bfloat16
+    # flat buffers, as a flat-parameter optimizer keeps them: the library then moves each chunk
+    # with one copy per direction
     host_g = []
     for s in range(2):
         gs = workloads.grads_torch(sizes, s + 1, w.grad_std, dev, kind=w.grad_kind, dtype=w.grad_dtype)
-        host_g.append([g.cpu().pin_memory() for g in gs])
+        _, views = workloads.flat_views(sizes, gdt, pin=True)
+        for v, g in zip(views, gs):
+            v.copy_(g)
+        host_g.append(views)
         del gs
-    host_p = [torch.empty(p.numel(), dtype=torch.float32, pin_memory=True) for p in params]
-    dev_g = [torch.empty(n, dtype=gdt, device=dev) for n in sizes]
+    _, host_p = workloads.flat_views(sizes, torch.float32, pin=True)
+    _, dev_g = workloads.flat_views(sizes, gdt, dev)
     h2d = sum(g.numel() * g.element_size() for g in host_g[0])
     d2h = sum(p.numel() * 4 for p in params)
     plan = psa.StepPlan(mode, params, dev_g, state, **kw)
@@ -458,15 +463,24 @@ def run_e2e(args, psa, torch, dev, stream, w, spec, params, state, kw, t, flush,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "h2d_plus_d2h_gbs": round((h2d + d2h) * steps / total_s / 1e9, 1),
             "host_link": {**link, "cap_gparams_per_s": round(cap, 3), "frac_of_cap": round(value / cap, 4),
-                          "how": "pinned cudaMemcpyAsync of the same buffers, CUDA events: grads up, params "
-                                 "down, and both at once on two streams"},
+                          "how": "pinned cudaMemcpyAsync over the same flat buffers, one copy per "
+                                 "direction: grads up, params down, and both at once on two streams"},
             "pipeline": f"psadam_step_from_host, {args.e2e_chunks} chunks on 3 streams" if piped else
                         "psadam_step_from_host, one stream"}
 
 
+def _span(views):
+    """The one contiguous range that back-to-back views cover (first start to last end)."""
+    base = views[0]
+    n = (views[-1].data_ptr() - base.data_ptr()) // base.element_size() + views[-1].numel()
+    return base.as_strided((n,), (1,))
+
+
 def host_link_rates(torch, dev, host_g, dev_g, params, host_p, reps: int = 3) -> dict:
-    """GB/s of pinned host<->device copies of the end-to-end leg's own buffers: uploads alone,
-    downloads alone, and both at once (two streams); best of `reps`."""
+    """GB/s of pinned host<->device copies over the end-to-end leg's own flat buffers, each
+    direction as one copy: uploads alone, downloads alone, and both at once (two streams);
+    best of `reps`."""
+    host_g, dev_g, params, host_p = [_span(host_g)], [_span(dev_g)], [_span(params)], [_span(host_p)]
     up_b = sum(g.numel() * g.element_size() for g in host_g)
     down_b = sum(p.numel() * 4 for p in params)
     s_up, s_down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)

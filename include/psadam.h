@@ -174,7 +174,9 @@ int adam_step_q8v(const psadam_list* list, float* const* m, uint8_t* const* v_co
  * (stream) and downloads (stream_out) overlap; NULL streams run it all on `stream`. Either
  * way the results are bit for bit those of one adam_step_* call over the whole list (a
  * slice keeps its tensor's element offsets and list position for stochastic rounding), and
- * `stream` is ordered after every copy when the call returns. */
+ * `stream` is ordered after every copy when the call returns. Within a chunk, consecutive
+ * tensors whose host and device buffers both lie back to back (flat buffers) are moved by
+ * one copy per direction. */
 int psadam_step_from_host(int32_t mode, const psadam_list* list, const void* const* host_grad,
                           float* const* host_param, void* const* m, void* const* v,
                           float* const* m_scale, float* const* v_scale, int64_t step,

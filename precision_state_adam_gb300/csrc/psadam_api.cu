@@ -174,6 +174,8 @@ int run_launches(const std::vector<Entry>& es, const StepConsts& c, uint64_t see
   a.seed_hi = (uint32_t)(seed >> 32);
   a.step_lo = (uint32_t)step;
   a.block_size = bs;
+  a.block_shift = 0;
+  while ((1 << a.block_shift) < bs && a.block_shift < 30) ++a.block_shift;
   a.tile = unit;
   a.k_full = percentile_rank(pct, bs);
   size_t i = 0;
@@ -242,9 +244,22 @@ Launcher<CAP> pick_step_any(int mode, bool gb, bool sr) {
 }
 
 template <int CAP>
+Launcher<CAP> pick_step_sub(int mode, bool gb, bool sr) {
+  if (mode == kModeQ8V) {
+    if (gb) return sr ? &launch_step_sub<kModeQ8V, true, true, CAP> : &launch_step_sub<kModeQ8V, true, false, CAP>;
+    return sr ? &launch_step_sub<kModeQ8V, false, true, CAP> : &launch_step_sub<kModeQ8V, false, false, CAP>;
+  }
+  if (gb) return sr ? &launch_step_sub<kModeQ8, true, true, CAP> : &launch_step_sub<kModeQ8, true, false, CAP>;
+  return sr ? &launch_step_sub<kModeQ8, false, true, CAP> : &launch_step_sub<kModeQ8, false, false, CAP>;
+}
+
+template <int CAP>
 Launcher<CAP> pick_quantize(bool sr, int K) {
-  if (sr) return K == 1 ? &launch_quantize<true, 1, CAP> : (K == 3 ? &launch_quantize<true, 3, CAP> : &launch_quantize<true, 4, CAP>);
-  return K == 1 ? &launch_quantize<false, 1, CAP> : (K == 3 ? &launch_quantize<false, 3, CAP> : &launch_quantize<false, 4, CAP>);
+  if (sr)
+    return K == 1 ? &launch_quantize<true, 1, CAP>
+                  : (K == 3 ? &launch_quantize<true, 3, CAP> : &launch_quantize<true, 4, CAP>);
+  return K == 1 ? &launch_quantize<false, 1, CAP>
+                : (K == 3 ? &launch_quantize<false, 3, CAP> : &launch_quantize<false, 4, CAP>);
 }
 
 // Dispatch on list length: short lists use the small parameter block.
@@ -333,6 +348,13 @@ int prepare_step(int mode, const psadam_list* list, const void* const* m, const 
 // depends only on each block's own elements, its tensor's last-block length and rank).
 int launch_prepared(const std::vector<Entry>& es, const StepCall& call, cudaStream_t s) {
   const int kmax = max_rank(es, call.pct, call.bs);
+  // Power-of-two blocks of 16..1024 elements at rank 1 without the runtime options: several
+  // blocks per tile of the persistent kernel
+  const bool pow2 = (call.bs & (call.bs - 1)) == 0;
+  const bool opts = call.gs.unscale != 1.0f || call.gs.zero != 0 || call.gs.static_scales != 0;
+  if (call.q8mode && pow2 && call.bs >= kMinSubBlock && call.bs <= kMaxSubBlock && kmax == 1 && !opts)
+    return dispatch(es, call.c, call.seed, call.step, call.pct, pick_step_sub<kCapSmall>(call.mode, call.gb, call.sr),
+                    pick_step_sub<kCapLarge>(call.mode, call.gb, call.sr), s, call.gs, call.bs, kBlock);
   // 2048-element blocks with rank <= kMaxRank: the specialised kernels; otherwise the general one
   if (call.q8mode && (call.bs != kBlock || kmax > kMaxRank))
     return dispatch(es, call.c, call.seed, call.step, call.pct, pick_step_any<kCapSmall>(call.mode, call.gb, call.sr),
@@ -376,6 +398,35 @@ int cuda_fail(cudaError_t e) {
   g_last_cuda_error = (int32_t)e;
   return PSADAM_ERR_CUDA;
 }
+
+// Copies of consecutive pieces merged while both the source and the destination continue
+// where the previous piece ended (tensors laid out back to back in flat buffers): one
+// cudaMemcpyAsync per run instead of one per tensor.
+struct CopyRun {
+  cudaMemcpyKind kind;
+  cudaStream_t stream;
+  char* dst = nullptr;
+  const char* src = nullptr;
+  size_t bytes = 0;
+  CopyRun(cudaMemcpyKind k, cudaStream_t s) : kind(k), stream(s) {}
+  cudaError_t add(void* d, const void* sp, size_t n) {
+    if (bytes != 0 && static_cast<char*>(d) == dst + bytes && static_cast<const char*>(sp) == src + bytes) {
+      bytes += n;
+      return cudaSuccess;
+    }
+    const cudaError_t e = flush();
+    dst = static_cast<char*>(d);
+    src = static_cast<const char*>(sp);
+    bytes = n;
+    return e;
+  }
+  cudaError_t flush() {
+    if (bytes == 0) return cudaSuccess;
+    const cudaError_t e = cudaMemcpyAsync(dst, src, bytes, kind, stream);
+    bytes = 0;
+    return e;
+  }
+};
 
 // A slice's first element / 4 reaches the kernels as an int (the stochastic-rounding counter
 // offset, TensorRef::grp_off), so no cut lies past 4 * INT_MAX elements of a tensor: the rest
@@ -466,11 +517,12 @@ int psadam_step_from_host(int32_t mode, const psadam_list* list, const void* con
       return cuda_fail(e);
   }
   for (size_t c = 0; c < chunks.size(); ++c) {
+    CopyRun up(cudaMemcpyHostToDevice, sin);
     for (const Entry& pc : chunks[c]) {
       const char* src = static_cast<const char*>(host_grad[pc.list_idx]) + pc.elem_off * (long long)gsz;
-      if ((e = cudaMemcpyAsync(const_cast<void*>(pc.g), src, pc.numel * gsz, cudaMemcpyHostToDevice, sin)) != cudaSuccess)
-        return cuda_fail(e);
+      if ((e = up.add(const_cast<void*>(pc.g), src, (size_t)pc.numel * gsz)) != cudaSuccess) return cuda_fail(e);
     }
+    if ((e = up.flush()) != cudaSuccess) return cuda_fail(e);
     if (piped) {
       if ((e = cudaEventRecord(ev[2 + 2 * c], sin)) != cudaSuccess || (e = cudaStreamWaitEvent(s, ev[2 + 2 * c], 0)) != cudaSuccess)
         return cuda_fail(e);
@@ -481,11 +533,12 @@ int psadam_step_from_host(int32_t mode, const psadam_list* list, const void* con
           (e = cudaStreamWaitEvent(sout, ev[3 + 2 * c], 0)) != cudaSuccess)
         return cuda_fail(e);
     }
+    CopyRun down(cudaMemcpyDeviceToHost, sout);
     for (const Entry& pc : chunks[c]) {
       float* dst = host_param[pc.list_idx] + pc.elem_off;
-      if ((e = cudaMemcpyAsync(dst, pc.p, pc.numel * sizeof(float), cudaMemcpyDeviceToHost, sout)) != cudaSuccess)
-        return cuda_fail(e);
+      if ((e = down.add(dst, pc.p, (size_t)pc.numel * sizeof(float))) != cudaSuccess) return cuda_fail(e);
     }
+    if ((e = down.flush()) != cudaSuccess) return cuda_fail(e);
   }
   // the caller's stream sees the whole step, downloads included
   if (piped) {

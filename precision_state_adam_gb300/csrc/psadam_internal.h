@@ -18,7 +18,8 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kCapSmall = 8;
 constexpr int kCapLarge = 440;
 // Largest percentile rank k the 2048-block kernels select (per-lane sorted top-K lists and
-// warp extraction; for higher ranks the general kernel's radix select measured faster).
+// warp extraction); higher ranks run the general kernel's radix select, which measured faster
+// than a top-16 network and than a per-warp bitwise search (about 31 compares per value).
 constexpr int kMaxRank = 4;
 // Largest quantization block of the any-block-size kernels (its fp32 m', v' are staged in
 // shared memory: 128 KB for both moments).
@@ -69,6 +70,7 @@ struct LaunchArgs {
   int* fault;       // device word set to 1 when a bounded wait gives up (see psadam_device_fault)
   int static_scales;  // 8-bit: a block's nonzero scale is kept instead of recomputed
   int block_size;     // 8-bit quantization block (the 2048-block kernels assume 2048)
+  int block_shift;    // log2(block_size) when it is a power of two (the sub-block path)
   int tile;           // elements per CTA (a whole number of blocks)
   int approx;         // nonzero: approximate square root and division in the update
   TensorRef t[CAP];
@@ -88,6 +90,13 @@ cudaError_t launch_quantize(const LaunchArgs<CAP>& a, cudaStream_t s);
 
 template <int CAP>
 cudaError_t launch_dequantize(const LaunchArgs<CAP>& a, cudaStream_t s);
+
+// Power-of-two block sizes in [kMinSubBlock, kMaxSubBlock] with rank 1 and the plain or
+// approximate update: the persistent kernel, several blocks per 2048-element tile.
+constexpr int kMinSubBlock = 16;
+constexpr int kMaxSubBlock = 1024;
+template <int MODE, bool GBF16, bool SR, int CAP>
+cudaError_t launch_step_sub(const LaunchArgs<CAP>& a, cudaStream_t s);
 
 // Any block size in [1, kMaxAnyBlock] and any percentile rank: one CTA per quantization block.
 template <int MODE, bool GBF16, bool SR, int CAP>

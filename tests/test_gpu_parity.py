@@ -135,8 +135,15 @@ def test_q8_step_ragged_list(psa, case, grad_dtype, mode, approx):
 
 
 # ------------------------------------------------------------------ any block size, any percentile
-# (the general kernel: one CTA per block, shared-memory staging, radix-select ranks)
+# Power-of-two blocks of 16..1024 elements at rank 1 (no runtime options) run in the persistent
+# kernel's 2048-element tiles as sub-blocks; the rest runs the general kernel (one CTA per tile
+# of whole blocks, shared-memory staging, radix-select ranks).
 ANY_CASES = {
+    "bs16_sr": (Q8Opts(True, 5, 100.0, block_size=16), [1, 15, 17, 2047, 2063, 9000]),
+    "bs32_rne": (Q8Opts(False, 42, 100.0, block_size=32), [31, 33, 4096, 5000]),
+    "bs128_sr_p99.9": (Q8Opts(True, 7, 99.9, block_size=128), [1, 127, 129, 6000]),   # rank 1 at 128
+    "bs512_p99.95": (Q8Opts(False, 42, 99.95, block_size=512), [511, 513, 2048, 9999]),  # rank 1 at 512
+    "bs1024_sr": (Q8Opts(True, 8, 100.0, block_size=1024), [1023, 1025, 3000, 70001]),
     "bs1_rne": (Q8Opts(False, 42, 100.0, block_size=1), [1, 2, 33, 300]),
     "bs3_sr": (Q8Opts(True, 42, 100.0, block_size=3), [1, 2, 7, 1000]),
     "bs64_rne": (Q8Opts(False, 42, 100.0, block_size=64), [1, 63, 64, 65, 5000]),
@@ -605,12 +612,15 @@ def test_steps_replay_from_a_cuda_graph(psa, mode):
         np.testing.assert_array_equal(a, b)
 
 
+@pytest.mark.parametrize("flat", [False, True])
 @pytest.mark.parametrize("piped", [False, True])
 @pytest.mark.parametrize("mode", ["fp32", "bf16m", "q8", "q8v", "q8/bs256", "q8/p99"])
-def test_step_from_host_equals_device_step(psa, mode, piped):
+def test_step_from_host_equals_device_step(psa, mode, piped, flat):
     """psadam_step_from_host (grads uploaded from pinned host buffers, params downloaded), in
     chunks pipelined over three streams or in one piece: the same bits as device-resident steps,
-    with stochastic rounding (slices keep their tensors' element offsets and list positions)."""
+    with stochastic rounding (slices keep their tensors' element offsets and list positions).
+    With `flat`, params, grads and the host buffers are views of flat buffers, so the library
+    merges the copies of back-to-back tensors."""
     base, _, rest = mode.partition("/")
     kw = dict(weight_decay=0.01)
     if base in ("q8", "q8v"):
@@ -627,14 +637,27 @@ def test_step_from_host_equals_device_step(psa, mode, piped):
     host_grads = []
     for t in (1, 2, 3):
         g = [torch.from_numpy(x) for x in workloads.grads_np(sizes, t, 1e-2, seed=29)]
-        host_grads.append([x.to(gdt).pin_memory() for x in g])
+        if flat:
+            _, hv = workloads.flat_views(sizes, gdt, pin=True)
+            for v, x in zip(hv, g):
+                v.copy_(x.to(gdt))
+            host_grads.append(hv)
+        else:
+            host_grads.append([x.to(gdt).pin_memory() for x in g])
     runs = []
     for from_host in (False, True):
-        params = _to_dev(p0)
+        if flat:
+            _, params = workloads.flat_views(sizes, torch.float32, DEV)
+            for v, a in zip(params, p0):
+                v.copy_(torch.from_numpy(a))
+            _, dev_g = workloads.flat_views(sizes, gdt, DEV)
+            _, out = workloads.flat_views(sizes, torch.float32, pin=True)
+        else:
+            params = _to_dev(p0)
+            dev_g = [torch.empty(n, dtype=gdt, device=DEV) for n in sizes]
+            out = [torch.empty(n, dtype=torch.float32).pin_memory() for n in sizes]
         state = psa.zeros_state(params, base, bs)
-        dev_g = [torch.empty(n, dtype=gdt, device=DEV) for n in sizes]
         plan = psa.StepPlan(base, params, dev_g, state, **kw)
-        out = [torch.empty(n, dtype=torch.float32).pin_memory() for n in sizes]
         s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
         for t in (1, 2, 3):
             if from_host:

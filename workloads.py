@@ -167,8 +167,31 @@ def random_moments_np(n: int, seed: int, m_std: float = 1e-3, v_scale: float = 1
 
 
 # ------------------------------------------------------------------ torch (device, for the bench)
-def init_params_torch(specs, device, seed: int = DEFAULT_SEED):
+def flat_views(sizes, dtype, device=None, pin: bool = False):
+    """Tensors of `sizes` elements laid out back to back in one buffer (as a flat-parameter
+    optimizer keeps them), each start rounded up to 16 bytes. Returns (buffer, views)."""
     import torch
+    esz = torch.empty((), dtype=dtype).element_size()
+    align = max(1, 16 // esz)
+    offs, cur = [], 0
+    for n in sizes:
+        offs.append(cur)
+        cur += -(-n // align) * align
+    if pin:
+        buf = torch.empty(max(cur, 1), dtype=dtype, pin_memory=True)
+    else:
+        buf = torch.empty(max(cur, 1), dtype=dtype, device=device)
+    return buf, [buf[o:o + n] for o, n in zip(offs, sizes)]
+
+
+def init_params_torch(specs, device, seed: int = DEFAULT_SEED, flat: bool = False):
+    """Parameters on `device`; with `flat`, views of one buffer (see flat_views)."""
+    import torch
+    if flat:
+        _, views = flat_views([s.numel for s in specs], torch.float32, device)
+        for v, t in zip(views, init_params_torch(specs, device, seed)):
+            v.copy_(t)
+        return views
     gen = torch.Generator(device=device)
     gen.manual_seed(seed)
     out = []
