@@ -1,14 +1,13 @@
-// Instantiations: any block size / any percentile rank (8-bit moments, both layouts).
+// Instantiations: any block size / any percentile rank, 8-bit m and v, round to nearest even;
+// quantize-only and dequantize-only for any block size.
 #include "psadam_kernels.cuh"
 
 namespace psadam {
-#define PSADAM_INST(MODE, GB, SR, CAP) template cudaError_t launch_step_any<MODE, GB, SR, CAP>(const LaunchArgs<CAP>&, cudaStream_t);
-#define PSADAM_INST_CAP(MODE, GB, SR) PSADAM_INST(MODE, GB, SR, kCapSmall) PSADAM_INST(MODE, GB, SR, kCapLarge)
-PSADAM_INST_CAP(kModeQ8, false, false)
-PSADAM_INST_CAP(kModeQ8, false, true)
-PSADAM_INST_CAP(kModeQ8, true, false)
-PSADAM_INST_CAP(kModeQ8, true, true)
-#undef PSADAM_INST_CAP
+#define PSADAM_INST(GB, CAP) template cudaError_t launch_step_any<kModeQ8, GB, false, CAP>(const LaunchArgs<CAP>&, cudaStream_t);
+PSADAM_INST(false, kCapSmall)
+PSADAM_INST(true, kCapSmall)
+PSADAM_INST(false, kCapLarge)
+PSADAM_INST(true, kCapLarge)
 #undef PSADAM_INST
 template cudaError_t launch_quantize_any<false, kCapSmall>(const LaunchArgs<kCapSmall>&, cudaStream_t);
 template cudaError_t launch_quantize_any<true, kCapSmall>(const LaunchArgs<kCapSmall>&, cudaStream_t);

@@ -4,7 +4,7 @@
 
 namespace psadam {
 #define PSADAM_INST(SR, K, CAP) template cudaError_t launch_quantize<SR, K, CAP>(const LaunchArgs<CAP>&, cudaStream_t);
-#define PSADAM_INST_K(SR, CAP) PSADAM_INST(SR, 1, CAP) PSADAM_INST(SR, 3, CAP) PSADAM_INST(SR, 4, CAP)
+#define PSADAM_INST_K(SR, CAP) PSADAM_INST(SR, 1, CAP) PSADAM_INST(SR, 3, CAP) PSADAM_INST(SR, 4, CAP) PSADAM_INST(SR, kRankSel, CAP)
 PSADAM_INST_K(false, kCapSmall)
 PSADAM_INST_K(true, kCapSmall)
 PSADAM_INST_K(false, kCapLarge)

@@ -220,7 +220,8 @@ Launcher<CAP> pick_step(int mode, bool gb, bool sr, int K) {
 #define PSADAM_PICK_K(MODE, GB, SR)                                 \
   if (K == 1) return PSADAM_STEP_FN(MODE, GB, SR, 1, CAP);          \
   if (K == 3) return PSADAM_STEP_FN(MODE, GB, SR, 3, CAP);          \
-  return PSADAM_STEP_FN(MODE, GB, SR, 4, CAP);
+  if (K == 4) return PSADAM_STEP_FN(MODE, GB, SR, 4, CAP);          \
+  return PSADAM_STEP_FN(MODE, GB, SR, kRankSel, CAP);
 #define PSADAM_PICK_MODE(MODE)                                      \
   if (gb) {                                                         \
     if (sr) { PSADAM_PICK_K(MODE, true, true) } else { PSADAM_PICK_K(MODE, true, false) } \
@@ -255,11 +256,14 @@ Launcher<CAP> pick_step_sub(int mode, bool gb, bool sr) {
 
 template <int CAP>
 Launcher<CAP> pick_quantize(bool sr, int K) {
-  if (sr)
-    return K == 1 ? &launch_quantize<true, 1, CAP>
-                  : (K == 3 ? &launch_quantize<true, 3, CAP> : &launch_quantize<true, 4, CAP>);
-  return K == 1 ? &launch_quantize<false, 1, CAP>
-                : (K == 3 ? &launch_quantize<false, 3, CAP> : &launch_quantize<false, 4, CAP>);
+  if (sr) {
+    if (K == 1) return &launch_quantize<true, 1, CAP>;
+    if (K == 3) return &launch_quantize<true, 3, CAP>;
+    return K == 4 ? &launch_quantize<true, 4, CAP> : &launch_quantize<true, kRankSel, CAP>;
+  }
+  if (K == 1) return &launch_quantize<false, 1, CAP>;
+  if (K == 3) return &launch_quantize<false, 3, CAP>;
+  return K == 4 ? &launch_quantize<false, 4, CAP> : &launch_quantize<false, kRankSel, CAP>;
 }
 
 // Dispatch on list length: short lists use the small parameter block.

@@ -17,10 +17,12 @@ constexpr int kWarps = kThreads / 32;
 // long lists the largest block that stays under the 32,764-byte parameter limit.
 constexpr int kCapSmall = 8;
 constexpr int kCapLarge = 440;
-// Largest percentile rank k the 2048-block kernels select (per-lane sorted top-K lists and
-// warp extraction); higher ranks run the general kernel's radix select, which measured faster
-// than a top-16 network and than a per-warp bitwise search (about 31 compares per value).
-constexpr int kMaxRank = 4;
+// Largest percentile rank k the 2048-block kernels select: ranks 2 and 3 by per-lane top-3
+// lists and warp extraction, rank 4 by top-4 lists, ranks 5..32 from sorted thread maxima and
+// a gathered candidate set (block_rank_stats); higher ranks run the general kernel's radix
+// select.
+constexpr int kMaxRank = 32;
+constexpr int kRankSel = 32;  // rank template of ranks 5..32
 // Largest quantization block of the any-block-size kernels (its fp32 m', v' are staged in
 // shared memory: 128 KB for both moments).
 constexpr int kMaxAnyBlock = 16384;
@@ -78,8 +80,8 @@ struct LaunchArgs {
 static_assert(sizeof(LaunchArgs<kCapLarge>) <= 32764, "kernel parameter block too large");
 
 // Rank templates: K = 1 (absmax), 3 (k-th largest for k = 2, 3: percentile 99.9 on full
-// blocks) or 4 (k = 4).
-constexpr int rank_template(int k) { return k <= 1 ? 1 : (k <= 3 ? 3 : 4); }
+// blocks), 4 (k = 4) or kRankSel (k = 5 .. 32: percentile 98.5 and up on full blocks).
+constexpr int rank_template(int k) { return k <= 1 ? 1 : (k <= 3 ? 3 : (k == 4 ? 4 : kRankSel)); }
 
 // Launchers, explicitly instantiated in the kernel translation units.
 template <int MODE, bool GBF16, bool SR, int K, int CAP>
