@@ -13,8 +13,8 @@
  * Sources of the method:
  *   - AiDotNet PR #814 "feat: add 8-bit Adam optimizer for memory efficiency":
  *     block-wise quantization with block size 2048 (options list: BlockSize, any
- *     positive size), signed codes for m and unsigned codes for v, scales recomputed every step ("dynamic quantization"),
- *     QuantizationPercentile (default 99.9, range 0..100) for outlier-aware scaling,
+ *     positive size), signed codes for m and unsigned codes for v, scales recomputed every step (its dynamic quantization),
+ *     QuantizationPercentile (default 99.9, range 0..100) so that outliers do not set the scale,
  *     optional stochastic rounding; its sequence diagram fixes the step order:
  *     dequantize m and v, Adam update with bias correction, quantize m, quantize v.
  *   - AiDotNet PR #1745 "perf(training): make BF16-Adam fused-compatible (proper bf16
@@ -155,7 +155,7 @@ int adam_step_q8(const psadam_list* list, int8_t* const* m_code, uint8_t* const*
                  const psadam_hparams* hp, const psadam_q8_opts* q8, void* stream);
 
 /* One AdamW step keeping the first moment in fp32 and only the second moment 8-bit (PR
- * #814's "Option to keep first moment in full precision (CompressBothMoments=false)").
+ * #814's option CompressBothMoments = false, which leaves the first moment in full precision).
  * m: device float[numel]; v_code: device uint8_t[numel]; v_scale: device
  * float[ceil(numel/block_size)]; all updated in place. v is encoded exactly as adam_step_q8
  * encodes it (same percentile rule, rounding and stochastic-rounding stream, moment 1). */

@@ -78,7 +78,7 @@ float orc_sr_uniform(uint64_t seed, int64_t step, int tensor_idx, int moment, in
 }
 
 /* ------------------------------------------------------------------------------ */
-/* bf16 moment storage — [P1745] "half-size ushort[] m/v buffers": a bf16 keeps    */
+/* bf16 moment storage — [P1745] keeps m and v in half-size 16-bit buffers: a bf16  */
 /* the top 16 bits of an fp32. Storing rounds to the nearer of the two bf16 values */
 /* around x, ties to the one with an even last bit; widening is exact.            */
 /* ------------------------------------------------------------------------------ */
@@ -155,7 +155,7 @@ orc_scalars orc_make_scalars(const orc_hparams* hp, int64_t t) {
  *   p' = p*(1 - lr*wd) - (lr/bc1) * m' / (sqrt(v')/sqrt(bc2) + eps)
  * which is p - lr*wd*p - lr * m_hat / (sqrt(v_hat) + eps) with m_hat = m'/bc1 and
  * v_hat = v'/bc2. The parameter update uses the unquantized m', v' ([P814] sequence
- * diagram: "Updated m, v, parameters" come back before Quantize(m), Quantize(v)). */
+ * diagram: the updated m, v and parameters come back before Quantize(m), Quantize(v)). */
 static void adam_element(float* p, float g, float* m, float* v, const orc_scalars* s) {
     float m_new = s->b1 * *m + s->omb1 * g;
     float v_new = s->b2 * *v + (s->omb2 * g) * g;
@@ -324,8 +324,8 @@ void orc_step_q8(int64_t n, float* p, const void* grad, int grad_bf16, int8_t* m
     }
 }
 
-/* [P814] summary: "Option to keep first moment in full precision
- * (CompressBothMoments=false)": m stays fp32, only v is block-quantized. Same step order
+/* [P814] summary: with CompressBothMoments = false the first moment stays in full
+ * precision: m stays fp32, only v is block-quantized. Same step order
  * (dequantize v, update, quantize v), same v encoding and stream as the 8-bit step. */
 void orc_step_q8v_block(int64_t cnt, int64_t elem0, float* p, const void* grad, int grad_bf16, float* m,
                         uint8_t* v_code, float* v_scale, const orc_hparams* hp, int64_t t,
