@@ -17,8 +17,9 @@ update (`modes`), and, under `workloads`, ViT-Base (86.5M params, every moment m
 2^30-param tensor with stochastic rounding and 99.9th-percentile scales, the general kernel
 on 16.7M params, and the 1M tensor as a latency. Inputs are synthetic and seeded
 (workloads.py) and resident in HBM before the timed region; up to 8 distinct grad sets are
-cycled. Between timed steps the L2 is flushed by writing a 384 MB buffer, outside the
-per-step CUDA events.
+cycled. Between timed steps the L2 is flushed, outside the per-step CUDA events: a 384 MB
+buffer is written and then read back, so the L2 holds none of the step's inputs and none of
+the flush's writes are still waiting to go to HBM when the step starts.
 
 value      = params updated per second over all ranks (Gparams/s), device-timed
 e2e        = the same through the public API with host buffers: each step copies its grads
@@ -225,6 +226,14 @@ def n_grad_sets(w: workloads.Workload, steps: int, warmup: int) -> int:
     return max(2, min(8, steps + warmup, GRAD_SET_BUDGET // max(per_set, 1)))
 
 
+def flush_l2(flush, t: int) -> None:
+    """Evict the L2 (129 MB) between timed steps: write the 384 MB buffer, then read it. The
+    read misses evict the written lines (their write-back happens here, not inside the next
+    step) and leave only clean lines of the buffer behind."""
+    flush.fill_(float(t))
+    flush.sum()
+
+
 def bench_workload(args, w: workloads.Workload, modes, rank: int, world: int, dist, dev, steps: int,
                    warmup: int, with_e2e: bool):
     """Device-timed steps of every mode of `modes` on workload `w`: per-step CUDA events on the
@@ -275,7 +284,7 @@ def bench_workload(args, w: workloads.Workload, modes, rank: int, world: int, di
             if pristine is not None:
                 for d, src in zip(grads[(t - 1) % n_sets], pristine[(t - 1) % n_sets]):
                     d.copy_(src)
-            flush.fill_(float(t))
+            flush_l2(flush, t)
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
             e0.record(stream)
@@ -444,7 +453,7 @@ def run_e2e(args, psa, torch, dev, stream, w, spec, params, state, kw, t, flush,
     ms = []
     for i in range(steps):
         t += 1
-        flush.fill_(float(t))
+        flush_l2(flush, t)
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
@@ -453,16 +462,23 @@ def run_e2e(args, psa, torch, dev, stream, w, spec, params, state, kw, t, flush,
         e1.synchronize()
         ms.append(e0.elapsed_time(e1))
     total_s = max_over_ranks(sum(ms) / 1e3, dist, dev)
+    # the link again after the steps (another tenant's host traffic can change it): the cap
+    # takes the faster of the two measurements of each direction
+    after = host_link_rates(torch, dev, host_g[0], dev_g, params, host_p)
+    best = {k: max(link[k], after[k]) for k in link}
     # the copies alone bound the step: at best the uploads and downloads of a step overlap
     # completely, each at its measured rate and both together at the both-ways rate
-    floor_s = max(h2d / (link["h2d_gbs"] * 1e9), d2h / (link["d2h_gbs"] * 1e9),
-                  (h2d + d2h) / (link["both_gbs"] * 1e9))
+    floor_s = max(h2d / (best["h2d_gbs"] * 1e9), d2h / (best["d2h_gbs"] * 1e9),
+                  (h2d + d2h) / (best["both_gbs"] * 1e9))
     value = job_gparams_per_s(sum(sizes), steps, total_s, world)
     cap = job_gparams_per_s(sum(sizes), 1, floor_s, world)
     return {"value": round(value, 3), "unit": "Gparams/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "h2d_plus_d2h_gbs": round((h2d + d2h) * steps / total_s / 1e9, 1),
-            "host_link": {**link, "cap_gparams_per_s": round(cap, 3), "frac_of_cap": round(value / cap, 4),
+            "step_ms": {"min": round(min(ms), 3), "median": round(statistics.median(ms), 3),
+                        "max": round(max(ms), 3)},
+            "host_link": {**link, "after_steps": after, "cap_gparams_per_s": round(cap, 3),
+                          "frac_of_cap": round(value / cap, 4),
                           "how": "pinned cudaMemcpyAsync over the same flat buffers, one copy per "
                                  "direction: grads up, params down, and both at once on two streams"},
             "pipeline": f"psadam_step_from_host, {args.e2e_chunks} chunks on 3 streams" if piped else
@@ -594,7 +610,8 @@ def workload_config(w: workloads.Workload, head: str, zero_grads: bool, steps: i
             "params": sum(w.sizes), "tensors": len(w.sizes), "grad_dtype": w.grad_dtype,
             "bytes_per_step": algorithmic_bytes(mode, w.sizes, w.grad_dtype, zero_grads,
                                                 over.get("block_size", 2048)),
-            "l2": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MB write outside the step events)",
+            "l2": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MB written, then read back, outside the "
+                  "step events)",
             "zero_grads": bool(zero_grads),
             "grads": f"{n_grad_sets(w, steps, warmup)} seeded sets resident in HBM, cycled"}
 

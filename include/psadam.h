@@ -227,6 +227,19 @@ int32_t psadam_device_fault(void);
  * [0, 2^31], the step kernels' own limit (PSADAM_ERR_INVALID_ARG otherwise). */
 int psadam_selftest_bounded_wait(int64_t cycles, void* stream);
 
+/* Self-test of the update's own square root and quotient. Where every moment of a thread's
+ * elements lies in [2^-60, 2^64] (with eps in [2^-60, 2^20]), the IEEE-exact step takes them
+ * from the hardware's reciprocal approximations plus one fused multiply-add correction each
+ * instead of IEEE sqrt and division; they must give the same bits. The call counts, on the
+ * device, the results that differ from IEEE sqrt / division: mismatches[0] over every float in
+ * [2^-102, 2^128) (root), [1] over pairs of significands a, b in [1, 2) (quotient; full = 1:
+ * all 2^46 pairs, about a minute; full = 0: 2^36 of them), [2] exponent-scaling checks of the
+ * approximations that extend [1] to every exponent of the domain, [3] the step's arithmetic
+ * on 2^25 random elements per setting of three (fused switch against the IEEE per-element
+ * update; p, m and v). Every count is 0 on a correct build. mismatches: host, 4 entries.
+ * Synchronous on `stream`. PSADAM_ERR_INVALID_ARG for a null array or full not 0/1. */
+int psadam_selftest_update_math(int32_t full, uint64_t* mismatches, void* stream);
+
 /* Static, human-readable name of a psadam_status value. */
 const char* psadam_status_string(int32_t status);
 

@@ -82,6 +82,8 @@ _lib.psadam_status_string.argtypes = [ctypes.c_int32]
 _lib.psadam_status_string.restype = ctypes.c_char_p
 _lib.psadam_selftest_bounded_wait.argtypes = [ctypes.c_int64, ctypes.c_void_p]
 _lib.psadam_selftest_bounded_wait.restype = ctypes.c_int
+_lib.psadam_selftest_update_math.argtypes = [ctypes.c_int32, ctypes.POINTER(ctypes.c_uint64), ctypes.c_void_p]
+_lib.psadam_selftest_update_math.restype = ctypes.c_int
 _lib.psadam_device_fault.argtypes = []
 _lib.psadam_device_fault.restype = ctypes.c_int32
 _lib.psadam_last_cuda_error.argtypes = []
@@ -452,6 +454,17 @@ class StepPlan:
                                         ctypes.cast(hp, _PP), *pp, step, ctypes.byref(self._hp), q8, n_chunks, h,
                                         sin, sout)
         _raise(st, f"StepPlan.step_from_host ({self.mode})")
+
+
+def selftest_update_math(full: bool = False, stream=None) -> dict:
+    """Device-side counts of results of the update's own root and quotient that differ from IEEE
+    sqrt / division (psadam_selftest_update_math): all four are 0 on a correct build."""
+    out = (ctypes.c_uint64 * 4)()
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    _raise(_lib.psadam_selftest_update_math(int(bool(full)), out, handle), "psadam_selftest_update_math")
+    return {"root": int(out[0]), "quotient": int(out[1]), "scaling": int(out[2]), "update": int(out[3])}
 
 
 def device_fault() -> int:

@@ -98,6 +98,8 @@ StepConsts make_consts(const psadam_hparams& hp, int64_t t) {
   c.step_size = (float)(lr / bc1);
   c.inv_sqrt_bc2 = (float)(1.0 / std::sqrt(bc2));
   c.eps = hp.eps;
+  // the domain of the update's own correctly rounded root and quotient (psadam_kernels.cuh)
+  c.fast_root = c.eps >= 0x1p-60f && c.eps <= 0x1p20f && c.inv_sqrt_bc2 >= 0x1p-20f && c.inv_sqrt_bc2 <= 0x1p20f;
   return c;
 }
 
@@ -686,6 +688,19 @@ int psadam_selftest_bounded_wait(int64_t cycles, void* stream) {
   if (fault == nullptr) return PSADAM_ERR_CUDA;
   const cudaError_t e = launch_wait_selftest(fault, cycles, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PSADAM_OK : cuda_fail(e);
+}
+
+int psadam_selftest_update_math(int32_t full, uint64_t* mismatches, void* stream) {
+  if (mismatches == nullptr || (full != 0 && full != 1)) return PSADAM_ERR_INVALID_ARG;
+  // three launches' constants: the pages' defaults at the first step, a late step of another
+  // setting, and eps = 0 (outside the fused domain: the IEEE path throughout)
+  psadam_hparams h0{1e-3f, 0.9f, 0.999f, 1e-8f, 0.01f}, h1{3e-4f, 0.9f, 0.95f, 1e-6f, 0.1f}, h2{1e-3f, 0.9f, 0.999f, 0.0f, 0.0f};
+  const StepConsts c[3] = {make_consts(h0, 1), make_consts(h1, 1000), make_consts(h2, 7)};
+  unsigned long long out[4] = {0, 0, 0, 0};
+  const cudaError_t e = launch_math_selftest(full, c, 3, out, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  for (int i = 0; i < 4; ++i) mismatches[i] = out[i];
+  return PSADAM_OK;
 }
 
 int32_t psadam_device_fault(void) {

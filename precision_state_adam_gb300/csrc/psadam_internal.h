@@ -39,6 +39,7 @@ enum Mode : int { kModeF32 = 0, kModeBF16 = 1, kModeQ8 = 2, kModeQ8V = 3 };  // 
 // Per-step fp32 constants (formed in double on the host, rounded once).
 struct StepConsts {
   float b1, omb1, b2, omb2, decay, step_size, inv_sqrt_bc2, eps;
+  int fast_root;  // eps and inv_sqrt_bc2 allow the update's fused root and quotient (adamw_n)
 };
 
 // One non-empty tensor of the list. For the quantize-only kernel p/g are unused and
@@ -112,6 +113,7 @@ cudaError_t launch_dequantize_any(const LaunchArgs<CAP>& a, cudaStream_t s);
 
 // Bounded-wait self-test: a wait that nothing completes gives up after `cycles`, sets *fault.
 cudaError_t launch_wait_selftest(int* fault, long long cycles, cudaStream_t s);
+cudaError_t launch_math_selftest(int full, const StepConsts* c, int n_c, unsigned long long* out, cudaStream_t s);
 
 // Non-finite grad check: sets *flag = 1 if any grad (times g_unscale) is inf or NaN.
 template <bool GBF16, int CAP>

@@ -173,6 +173,10 @@ def test_selftest_and_fault_validation(psa):
     # no wait longer than the step kernels' own limit (2^31 SM cycles, about a second)
     assert lib.psadam_selftest_bounded_wait((1 << 31) + 1, None) == psa.ERR_INVALID_ARG
     assert lib.psadam_selftest_bounded_wait(2 ** 62, None) == psa.ERR_INVALID_ARG
+    out = (ctypes.c_uint64 * 4)()
+    assert lib.psadam_selftest_update_math(0, None, None) == psa.ERR_INVALID_ARG
+    assert lib.psadam_selftest_update_math(2, out, None) == psa.ERR_INVALID_ARG
+    assert lib.psadam_selftest_update_math(-1, out, None) == psa.ERR_INVALID_ARG
 
 
 def test_binding_refuses_short_pointer_tables(psa):
