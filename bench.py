@@ -476,7 +476,7 @@ def run_e2e(args, psa, torch, dev, stream, w, spec, params, state, kw, t, flush,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "h2d_plus_d2h_gbs": round((h2d + d2h) * steps / total_s / 1e9, 1),
             "step_ms": {"min": round(min(ms), 3), "median": round(statistics.median(ms), 3),
-                        "max": round(max(ms), 3)},
+                        "max": round(max(ms), 3), "all": [round(x, 2) for x in ms]},
             "host_link": {**link, "after_steps": after, "cap_gparams_per_s": round(cap, 3),
                           "frac_of_cap": round(value / cap, 4),
                           "how": "pinned cudaMemcpyAsync over the same flat buffers, one copy per "
