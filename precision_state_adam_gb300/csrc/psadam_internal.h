@@ -33,6 +33,12 @@ constexpr int kAnyTile = 2048;
 constexpr int any_blocks_per_tile(int B) {
   return B >= kAnyTile ? 1 : (kAnyTile / B < kAnyMaxQ ? kAnyTile / B : kAnyMaxQ);
 }
+// Blocks larger than the general kernel's tile with absmax scales (rank 1), whose C channels
+// would take more than 32 KB of staging (fewer than 4 CTAs per SM), are not staged in shared
+// memory: the kernel reads each block twice instead (moments, then the whole update).
+__host__ __device__ constexpr bool any_recompute(int tile, int k_full, int channels) {
+  return tile > kAnyTile && k_full == 1 && tile * channels > 8192;
+}
 
 enum Mode : int { kModeF32 = 0, kModeBF16 = 1, kModeQ8 = 2, kModeQ8V = 3 };  // Q8V: fp32 m, 8-bit v
 

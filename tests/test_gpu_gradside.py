@@ -71,6 +71,38 @@ def test_grad_unscale_matches_oracle(psa, mode, unscale, bf16):
 
 
 @pytest.mark.parametrize("bf16", [False, True])
+@pytest.mark.parametrize("mode", ["q8", "q8v"])
+def test_grad_side_on_blocks_larger_than_a_tile(psa, mode, bf16):
+    """Blocks of 16384 with absmax scales: the general kernel reads each block twice (the
+    moments for the block maxima, then the whole update). The loss-scale removal must enter
+    both reads alike and the zeroing must follow the second: params, moments, codes and
+    scales match the oracle bit for bit, and the grads end zero."""
+    hp = HParams(weight_decay=0.01)
+    bs = 16384
+    q8 = Q8Opts(False, 42, 100.0, block_size=bs)
+    sizes = [1, 16383, 16385, 40000]
+    specs = [workloads.TensorSpec(f"t{i}", (n,)) for i, n in enumerate(sizes)]
+    p_host = workloads.init_params_np(specs, seed=47)
+    params = _dev(p_host)
+    state = psa.zeros_state(params, mode, bs)
+    ostate = host_state(mode, sizes, bs)
+    u = float(np.float32(1.0 / 3.0))
+    for t in (1, 2, 3):
+        g = [x * np.float32(1024.0) for x in workloads.grads_np(sizes, t, 1e-2, seed=48)]
+        g_host = [workloads.to_bf16_bits_truncate(x) for x in g] if bf16 else [x.astype(np.float32) for x in g]
+        grads = _dev(g_host)
+        kw = hp_kwargs(hp)
+        kw.update(q8_kwargs(q8))
+        psa.adam_step(mode, params, grads, state, t, grad_unscale=u, zero_grads=True, **kw)
+        oracle.step_list(mode, p_host, [oracle.unscale_grads(x, u) for x in g_host], ostate, t, hp, q8)
+        torch.cuda.synchronize()
+        assert all(int(torch.count_nonzero(x)) == 0 for x in grads)
+    for i in range(len(sizes)):
+        got = [params[i].cpu().numpy(), *device_state_to_host(mode, state, i)]
+        assert exact_fraction(mode, got, [p_host[i], *ostate[i]]) == 1.0, (mode, i)
+
+
+@pytest.mark.parametrize("bf16", [False, True])
 @pytest.mark.parametrize("mode", MODES)
 def test_zero_grads_zeroes_after_use(psa, mode, bf16):
     specs = [workloads.TensorSpec(f"t{i}", (n,)) for i, n in enumerate(SIZES)]

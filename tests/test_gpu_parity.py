@@ -151,7 +151,9 @@ ANY_CASES = {
     "bs256_static": (Q8Opts(False, 42, 100.0, True, block_size=256), [5, 256, 70001]),
     "bs1000_p90": (Q8Opts(False, 42, 90.0, block_size=1000), [17, 999, 1000, 1001, 12345]),
     "bs4096_sr_p99.9": (Q8Opts(True, 3, 99.9, block_size=4096), [1, 4095, 4097, 20000]),
-    "bs16384_rne": (Q8Opts(False, 42, 100.0, block_size=16384), [1, 16383, 16385, 40000]),
+    "bs16384_rne": (Q8Opts(False, 42, 100.0, block_size=16384), [1, 16383, 16385, 40000]),  # read twice
+    "bs8192_sr": (Q8Opts(True, 13, 100.0, block_size=8192), [1, 8191, 8193, 30000]),        # q8: read twice
+    "bs8192_static": (Q8Opts(False, 42, 100.0, True, block_size=8192), [5, 8192, 24577]),
     "bs2048_p90": (Q8Opts(False, 42, 90.0), RAGGED),            # rank 205: general kernel at 2048
     "bs2048_sr_p50": (Q8Opts(True, 11, 50.0), [1, 2047, 2049, 9000]),
     "bs2048_p99_static": (Q8Opts(False, 42, 99.0, True), [3000, 2048]),
