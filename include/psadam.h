@@ -26,14 +26,16 @@
  *   m' = beta1*m + (1-beta1)*g
  *   v' = beta2*v + ((1-beta2)*g)*g
  *   p' = p*(1 - lr*wd) - (lr/bc1) * (m' / (sqrt(v')*(1/sqrt(bc2)) + eps))
- * By default every operation is IEEE-exact. psadam_list.approx_update opts into the
- * hardware's approximate fp32 square root and quotient in p' (relative errors within 2^-23
- * and 2 ulp): p' then lands within a few ulp of the update term of the exact value (close
- * normwise, not elementwise-relative where p' passes near zero), while m', v' and every
- * stored moment, code and scale stay exact; the 8-bit step is about 10 % faster.
  * with bc1 = 1 - beta1^step and bc2 = 1 - beta2^step; the per-step constants
  * (1-beta1), (1-beta2), 1 - lr*wd, lr/bc1 and 1/sqrt(bc2) are formed in double on the
- * host and rounded once to fp32. bf16 moments are widened exactly before and rounded to
+ * host and rounded once to fp32. By default every operation is IEEE-exact (the square root
+ * and the quotient come from a fused correctly rounded pair inside a checked domain, with
+ * the same bits as IEEE sqrt and division; see psadam_selftest_update_math).
+ * psadam_list.approx_update opts into the hardware's approximate fp32 square root and
+ * quotient in p' (relative errors within 2^-23 and 2 ulp): p' then lands within a few ulp
+ * of the update term of the exact value (close normwise, not elementwise-relative where p'
+ * passes near zero), while m', v' and every stored moment, code and scale stay exact; the
+ * 8-bit step is 2-3 % faster. bf16 moments are widened exactly before and rounded to
  * nearest even after. 8-bit moments are decoded as code*scale, the update uses the
  * unquantized m', v', and each block of B elements (default 2048) is then re-encoded:
  *   X_m = k-th largest |m'| of the block, X_v = k-th largest v' (k = 1 for absmax)
@@ -93,10 +95,14 @@ typedef struct {
 } psadam_hparams;
 
 /* 8-bit options (PR #814's BlockSize, UseStochasticRounding, QuantizationPercentile).
- * Speed: block_size 2048 with a rank k <= 4 (percentile >= 99.81 on full blocks; 100 and
- * the default 99.9 included) runs the specialised 2048-block kernels; any other block size
- * or a lower percentile runs a general kernel (tiles of whole blocks, shared-memory
- * staging, radix select) with identical results for identical inputs, only slower. */
+ * Speed (identical results on every path for identical inputs):
+ *   - block_size 2048 with a rank k <= 32 (percentile >= 98.5 on full blocks; 100 and the
+ *     default 99.9 included) runs the pipelined 2048-block kernels, fastest at k <= 4;
+ *   - power-of-two block sizes 16..1024 at rank 1 (absmax, or any percentile whose rank is
+ *     1 at that size) and without grad-side options run as sub-blocks of the same kernels;
+ *   - anything else runs a general kernel (tiles of whole blocks, shared-memory staging,
+ *     radix select for ranks above 1). Blocks above 2048 with absmax scales whose staging
+ *     would pass 32 KB are read twice instead of staged. */
 typedef struct {
     int32_t block_size;          /* elements per block, 1..16384 (INVALID_ARG below 1,
                                     UNSUPPORTED above); PR #814's default is 2048 */

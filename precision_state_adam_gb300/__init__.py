@@ -206,7 +206,7 @@ def adam_step_fp32(params, grads, m, v, step: int, lr: float = 1e-3, beta1: floa
     after use when ``zero_grads``, and the whole step is skipped on the device when the
     CUDA int32 tensor ``skip_flag`` holds a nonzero value (see :func:`check_grads`).
     ``approx_update`` opts into the hardware's approximate square root and quotient in the
-    parameter update (about 10 % faster for 8-bit moments; params within a few ulp of the
+    parameter update (2-3 % faster for 8-bit moments; params within a few ulp of the
     update of the IEEE result, every moment, code and scale still exact)."""
     lst, keep = _list(params, grads, grad_unscale, zero_grads, skip_flag, approx_update=approx_update)
     _check_layout("m", m, torch.float32, params)
