@@ -89,11 +89,43 @@ def algorithmic_bytes(mode: str, sizes, grad_dtype: str, zero_grads: bool = Fals
     return total
 
 
-def kernel_source_hash() -> str:
+def _code_only(text: str) -> str:
+    """C/C++/CUDA source without comments and with whitespace runs collapsed: what the
+    compiler sees of it (string and character literals are left alone)."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":  # a literal: copy it to its closing quote
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
+def kernel_source_hash(sources: dict | None = None) -> str:
+    """Hash of the kernel sources (csrc/) as the compiler sees them: an edit to a comment
+    keeps it, so the stored ncu traffic stays attached to the code it measured.
+    sources: {file name: text} to hash instead of the files on disk."""
+    if sources is None:
+        sources = {}
+        for f in sorted(glob.glob(os.path.join(ROOT, "precision_state_adam_gb300", "csrc", "*"))):
+            with open(f, encoding="utf-8") as fh:
+                sources[os.path.basename(f)] = fh.read()
     h = hashlib.sha256()
-    for f in sorted(glob.glob(os.path.join(ROOT, "precision_state_adam_gb300", "csrc", "*"))):
-        with open(f, "rb") as fh:
-            h.update(os.path.basename(f).encode() + fh.read())
+    for name in sorted(sources):
+        h.update(name.encode() + b"\0" + _code_only(sources[name]).encode())
     return h.hexdigest()[:16]
 
 

@@ -118,3 +118,15 @@ def test_grad_sets_stay_within_budget():
         per = sum(w.sizes) * (4 if w.grad_dtype == "f32" else 2)
         assert 2 <= n <= 8
         assert n == 2 or n * per <= bench.GRAD_SET_BUDGET, name
+
+
+def test_kernel_hash_ignores_comments_not_code():
+    """The stored ncu traffic stays attached to a kernel through comment edits only."""
+    base = {"k.cu": 'int f(int x) {  // twice\n  return 2 * x; /* doubled */ }\nconst char* s = "a // b";\n'}
+    same = {"k.cu": 'int f(int x) {\n  // a new remark\n  return 2 * x;   }\nconst char* s = "a // b";\n'}
+    code = {"k.cu": 'int f(int x) {  // twice\n  return 3 * x; /* doubled */ }\nconst char* s = "a // b";\n'}
+    lit = {"k.cu": 'int f(int x) {  // twice\n  return 2 * x; /* doubled */ }\nconst char* s = "a / b";\n'}
+    h = bench.kernel_source_hash(base)
+    assert bench.kernel_source_hash(same) == h
+    assert bench.kernel_source_hash(code) != h
+    assert bench.kernel_source_hash(lit) != h
