@@ -482,7 +482,9 @@ def run_e2e(args, psa, torch, dev, stream, w, spec, params, state, kw, t, flush,
     torch.cuda.synchronize(dev)
     if dist is not None:
         dist.barrier()
-    ms = []
+    # the steps are queued back to back with no host wait between them, as a training loop
+    # issues them: a host thread that stalls for a moment does not leave the link idle
+    evs = []
     for i in range(steps):
         t += 1
         flush_l2(flush, t)
@@ -491,8 +493,9 @@ def run_e2e(args, psa, torch, dev, stream, w, spec, params, state, kw, t, flush,
         e0.record(stream)
         one_step(i % 2, t)
         e1.record(stream)
-        e1.synchronize()
-        ms.append(e0.elapsed_time(e1))
+        evs.append((e0, e1))
+    torch.cuda.synchronize(dev)
+    ms = [a.elapsed_time(b) for a, b in evs]
     total_s = max_over_ranks(sum(ms) / 1e3, dist, dev)
     # the link again after the steps (another tenant's host traffic can change it): the cap
     # takes the faster of the two measurements of each direction
