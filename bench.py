@@ -121,8 +121,9 @@ def kernel_source_hash(sources: dict | None = None) -> str:
     if sources is None:
         sources = {}
         for f in sorted(glob.glob(os.path.join(ROOT, "precision_state_adam_gb300", "csrc", "*"))):
-            with open(f, encoding="utf-8") as fh:
-                sources[os.path.basename(f)] = fh.read()
+            if f.endswith((".cu", ".cuh", ".h")):
+                with open(f, encoding="utf-8", errors="replace") as fh:
+                    sources[os.path.basename(f)] = fh.read()
     h = hashlib.sha256()
     for name in sorted(sources):
         h.update(name.encode() + b"\0" + _code_only(sources[name]).encode())
