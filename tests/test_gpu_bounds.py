@@ -8,8 +8,9 @@ the same way from one pinned host allocation. This stands in for a memory checke
 tensors (partial stores, zero-filled copies past a tensor's end, bulk copies limited to full
 blocks) and slices of the host pipeline all write close to buffer ends.
 
-Sizes 1, 7, 2047, 2049 and 4097 go in one list per call, at block sizes 3, 16, 100, 256, 2048
-and 4096 (16 and 256 take the persistent kernel's sub-block path), for every moment mode with
+Sizes 1, 7, 2047, 2049 and 4097 go in one list per call, at block sizes 3, 16, 100, 256, 2048,
+4096 and 16384 (16 and 256 take the persistent kernel's sub-block path; 16384 with absmax
+scales the general kernel's read-twice path), for every moment mode with
 its options (stochastic rounding with percentile scales, grad zeroing, static scales, bf16
 grads, the approximate update), and for quantize-only,
 dequantize-only, the grad check and the host pipeline. Each step is also checked against the
@@ -31,7 +32,8 @@ from parity_util import hp_kwargs, host_state
 pytestmark = pytest.mark.gpu
 
 SIZES = [1, 7, 2047, 2049, 4097]
-BLOCKS = [3, 16, 100, 256, 2048, 4096]  # 16 and 256: sub-blocks of the persistent kernel
+# 16 and 256: sub-blocks of the persistent kernel; 16384 with absmax scales: read twice, not staged
+BLOCKS = [3, 16, 100, 256, 2048, 4096, 16384]
 GUARD = 64
 PATTERN = 0xA5
 DEV = "cuda:0"
